@@ -1,0 +1,272 @@
+"""Seeded synthetic inputs for the hybrid sparse MQA attention step.
+
+This module only draws random numbers and lays them out the way the step reads
+them: query rows, per-head sinks, paged KV pools with their page tables,
+sequence lengths, query boundaries and top-k index lists.  It holds none of
+the step's arithmetic, so both the CUDA path and the float64 oracle can take
+their inputs from it.
+
+The FP8 packer below produces the packed KV rows that the cache writer would
+store (448 e4m3 nope values, 64 bf16 rope values, 7 fp32 scales, 608-byte
+stride); that writer is outside the attention step, so for the step these rows
+are generated inputs.
+
+Shapes follow the five workloads of the step:
+  swa_tiny       batch 2, seq_lens (7,7), H=8, SWA only
+  swa_decode     batch 64, H=64, seq_len uniform 2K..32K, SWA only, all pages
+                 resident and randomly permuted
+  c4_decode      batch 32, H=64, context 65536 (16384 compressed rows), 512
+                 distinct uniform indices per token
+  c128_decode    batch 16, H=128, context 1,048,576 (8192 compressed rows, all
+                 attended)
+  c4_verify_fp8  batch 64 x 4 query tokens, H=64, context 262144, top-512,
+                 packed FP8 KV
+Values: q and KV ~ N(0,1)*0.5 in bf16, sink ~ N(0,1) in fp32,
+scale = 1/sqrt(512).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+
+import numpy as np
+import torch
+
+PAGE = 256
+DIM = 512
+NOPE = 448
+ROPE = 64
+BLOCK = 64
+FP8_STRIDE = 608
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    batch: int
+    heads: int
+    ratio: int = 0                 # 0 = SWA only, 4 = C4 top-k, 128 = C128 dense
+    window: int = 128
+    topk: int = 512
+    seq_lens: tuple | None = None  # fixed lengths, else drawn from seq_range
+    seq_range: tuple = (0, 0)
+    qlen: int = 1                  # query tokens per request (verify when > 1)
+    kv_format: str = "bf16"        # "bf16" or "fp8"
+    swa_resident: str = "window"   # "window": only pages the window touches; "all"
+    req_pool_indices: tuple | None = None
+    decoy_pages: int = 4           # unused pool pages with random content
+    seed: int = 0
+
+    @property
+    def tokens(self):
+        return self.batch * self.qlen
+
+
+PRESETS = {
+    "swa_tiny": Workload("swa_tiny", batch=2, heads=8, seq_lens=(7, 7),
+                         req_pool_indices=(5, 9), decoy_pages=3, seed=0),
+    "swa_decode": Workload("swa_decode", batch=64, heads=64, seq_range=(2048, 32768),
+                           swa_resident="all", seed=1),
+    "c4_decode": Workload("c4_decode", batch=32, heads=64, ratio=4,
+                          seq_lens=(65536,) * 32, seed=2),
+    "c128_decode": Workload("c128_decode", batch=16, heads=128, ratio=128,
+                            seq_lens=(1048576,) * 16, seed=3),
+    "c4_verify_fp8": Workload("c4_verify_fp8", batch=64, heads=64, ratio=4,
+                              seq_lens=(262144,) * 64, qlen=4, kv_format="fp8", seed=4),
+}
+
+
+@dataclass
+class Inputs:
+    """One batch of step inputs (torch tensors on one device)."""
+    work: Workload
+    q: torch.Tensor                     # [T, H, 512] bf16
+    sink: torch.Tensor                  # [H] fp32
+    seq_lens: torch.Tensor              # [B] int32
+    cu_seqlens_q: torch.Tensor | None   # [B+1] int32, None for decode
+    req_pool_indices: torch.Tensor | None
+    swa_pool: torch.Tensor              # [rows, 512] bf16 or [rows, 608] uint8
+    swa_page_table: torch.Tensor        # [R, P] int32
+    extra_pool: torch.Tensor | None
+    extra_page_table: torch.Tensor | None
+    topk_idx: torch.Tensor | None       # [T, topk] int32
+    scale: float = 1.0 / math.sqrt(DIM)
+    max_seq_len: int = 0
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def T(self):
+        return self.q.shape[0]
+
+    @property
+    def H(self):
+        return self.q.shape[1]
+
+    def to(self, device):
+        def mv(x):
+            return None if x is None else x.to(device)
+        return replace(self, q=mv(self.q), sink=mv(self.sink), seq_lens=mv(self.seq_lens),
+                       cu_seqlens_q=mv(self.cu_seqlens_q),
+                       req_pool_indices=mv(self.req_pool_indices),
+                       swa_pool=mv(self.swa_pool), swa_page_table=mv(self.swa_page_table),
+                       extra_pool=mv(self.extra_pool),
+                       extra_page_table=mv(self.extra_page_table),
+                       topk_idx=mv(self.topk_idx))
+
+    def oracle_kwargs(self):
+        """numpy views of every input, in the oracle's argument names."""
+        def np_(x):
+            return None if x is None else x.detach().cpu().numpy()
+        def bits(x):
+            if x is None:
+                return None
+            x = x.detach().cpu()
+            if x.dtype == torch.bfloat16:
+                return x.view(torch.int16).numpy().view(np.uint16)
+            return x.numpy()
+        return dict(
+            q_bits=bits(self.q), sink=np_(self.sink), scale=self.scale,
+            seq_lens=np_(self.seq_lens), window=self.work.window,
+            swa_pool=bits(self.swa_pool), swa_page_table=np_(self.swa_page_table),
+            kv_format=self.work.kv_format, compress_ratio=self.work.ratio,
+            extra_pool=bits(self.extra_pool), extra_page_table=np_(self.extra_page_table),
+            topk_idx=np_(self.topk_idx), cu_seqlens_q=np_(self.cu_seqlens_q),
+            req_pool_indices=np_(self.req_pool_indices))
+
+
+# --------------------------------------------------------------------------
+def pack_fp8_rows(rows_bf16: torch.Tensor) -> torch.Tensor:
+    """bf16 [n, 512] -> packed uint8 [n, 608]: per 64-value nope block,
+    scale = amax / 448 (1 when the block is all zero), codes = round-to-nearest
+    e4m3 of value / scale; rope kept as bf16; scales stored as fp32."""
+    n = rows_bf16.shape[0]
+    x = rows_bf16.float()
+    nope = x[:, :NOPE].reshape(n, NOPE // BLOCK, BLOCK)
+    amax = nope.abs().amax(dim=2)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    codes = (nope / scale[:, :, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    out = torch.zeros(n, FP8_STRIDE, dtype=torch.uint8, device=rows_bf16.device)
+    out[:, :NOPE] = codes.reshape(n, NOPE).view(torch.uint8)
+    out[:, NOPE:NOPE + 2 * ROPE] = rows_bf16[:, NOPE:].contiguous().view(torch.uint8).reshape(n, 2 * ROPE)
+    out[:, NOPE + 2 * ROPE:NOPE + 2 * ROPE + 4 * (NOPE // BLOCK)] = \
+        scale.contiguous().view(torch.uint8).reshape(n, 4 * (NOPE // BLOCK))
+    return out
+
+
+def _randn_bf16(shape, gen, device, chunk_rows=1 << 20):
+    """N(0,1)*0.5 in bf16, drawn in chunks to bound temporary fp32 memory."""
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    flat = out.view(shape[0], -1)
+    for r0 in range(0, shape[0], chunk_rows):
+        r1 = min(shape[0], r0 + chunk_rows)
+        flat[r0:r1] = (torch.randn((r1 - r0, flat.shape[1]), generator=gen, device=device) * 0.5).to(torch.bfloat16)
+    return out
+
+
+def _pool(num_rows, kv_format, gen, device):
+    if kv_format == "bf16":
+        return _randn_bf16((num_rows, DIM), gen, device)
+    out = torch.empty(num_rows, FP8_STRIDE, dtype=torch.uint8, device=device)
+    step = 1 << 18
+    for r0 in range(0, num_rows, step):
+        r1 = min(num_rows, r0 + step)
+        out[r0:r1] = pack_fp8_rows(_randn_bf16((r1 - r0, DIM), gen, device))
+    return out
+
+
+def _page_tables(needed, num_req_rows, width, decoys, gen_cpu):
+    """Assign a random distinct physical page to every (request row, logical
+    page) in `needed`; pages not needed stay -1.  Returns (table, num_pages)."""
+    total = len(needed) + decoys
+    perm = torch.randperm(total, generator=gen_cpu).tolist()
+    table = torch.full((num_req_rows, max(width, 1)), -1, dtype=torch.int32)
+    for k, (r, lp) in enumerate(needed):
+        table[r, lp] = perm[k]
+    return table, total
+
+
+def make_inputs(work: Workload | str, device="cpu", seed=None, **overrides) -> Inputs:
+    """Draw one batch of inputs for a workload (a preset name or a Workload)."""
+    if isinstance(work, str):
+        work = PRESETS[work]
+    if overrides:
+        work = replace(work, **overrides)
+    if seed is not None:
+        work = replace(work, seed=seed)
+    gen_cpu = torch.Generator().manual_seed(work.seed)
+    dev = torch.device(device)
+    gen_dev = gen_cpu if dev.type == "cpu" else torch.Generator(device=dev).manual_seed(work.seed)
+
+    B, H = work.batch, work.heads
+    if work.seq_lens is not None:
+        seq = [int(s) for s in work.seq_lens]
+        assert len(seq) == B
+    else:
+        lo, hi = work.seq_range
+        seq = torch.randint(lo, hi + 1, (B,), generator=gen_cpu).tolist()
+    qlen = work.qlen
+    T = B * qlen
+    cu = None if qlen == 1 else torch.arange(0, T + 1, qlen, dtype=torch.int32)
+    rpi = work.req_pool_indices
+    table_rows = [b if rpi is None else rpi[b] for b in range(B)]
+    num_req_rows = (max(table_rows) + 1) if table_rows else 1
+
+    # ---- SWA pool: pages covering each request's windows (or every page).
+    needed = []
+    width = 0
+    for b in range(B):
+        p_max = seq[b] - 1
+        p_min = seq[b] - qlen
+        first = 0 if work.swa_resident == "all" else max(0, p_min - work.window + 1) // PAGE
+        last = p_max // PAGE
+        width = max(width, last + 1)
+        needed += [(table_rows[b], lp) for lp in range(first, last + 1)]
+    swa_table, swa_pages = _page_tables(needed, num_req_rows, width, work.decoy_pages, gen_cpu)
+    swa_pool = _pool(swa_pages * PAGE, work.kv_format, gen_dev, dev)
+
+    # ---- extra (compressed) pool: every compressed row of every request.
+    extra_pool = extra_table = topk = None
+    if work.ratio:
+        needed = []
+        width = 0
+        for b in range(B):
+            n_c = seq[b] // work.ratio
+            pages = (n_c + PAGE - 1) // PAGE
+            width = max(width, pages)
+            needed += [(table_rows[b], lp) for lp in range(pages)]
+        extra_table, extra_pages = _page_tables(needed, num_req_rows, width, work.decoy_pages, gen_cpu)
+        extra_pool = _pool(extra_pages * PAGE, work.kv_format, gen_dev, dev)
+    if work.ratio == 4:
+        topk = _topk_lists(seq, qlen, work.topk, gen_cpu)
+
+    q = _randn_bf16((T, H, DIM), gen_dev, dev)
+    sink = torch.randn(H, generator=gen_cpu).float()
+    inp = Inputs(work=work, q=q, sink=sink,
+                 seq_lens=torch.tensor(seq, dtype=torch.int32),
+                 cu_seqlens_q=cu,
+                 req_pool_indices=None if rpi is None else torch.tensor(rpi, dtype=torch.int32),
+                 swa_pool=swa_pool, swa_page_table=swa_table,
+                 extra_pool=extra_pool, extra_page_table=extra_table, topk_idx=topk,
+                 max_seq_len=max(seq) if seq else 0)
+    return inp.to(dev)
+
+
+def _topk_lists(seq, qlen, topk, gen_cpu):
+    """Per query token: min(topk, n_c) distinct uniform indices in [0, n_c(p)),
+    unsorted, padded with -1 (n_c(p) = (p+1)//4 compressed rows are visible)."""
+    rows = []
+    for s in seq:
+        for i in range(qlen):
+            p = s - qlen + i
+            n_c = (p + 1) // 4
+            k = min(topk, n_c)
+            if n_c <= 4 * topk:
+                pick = torch.randperm(n_c, generator=gen_cpu)[:k]
+            else:
+                # rejection-free distinct draw: random keys, keep the k largest
+                pick = torch.rand(n_c, generator=gen_cpu).topk(k).indices
+                pick = pick[torch.randperm(k, generator=gen_cpu)]
+            row = torch.full((topk,), -1, dtype=torch.int32)
+            row[:k] = pick.to(torch.int32)
+            rows.append(row)
+    return torch.stack(rows) if rows else torch.zeros((0, topk), dtype=torch.int32)

@@ -1,0 +1,379 @@
+"""Checks that tie the float64 oracle to things other than itself.
+
+Each pin_* function raises AssertionError when the oracle disagrees with a
+closed form, a brute-force evaluation, a library routine, or the worked
+request-mapping example printed on "DeepSeek-V4 Attention: Query, Cache Write
+and History Addressing" (sections 1 and 4).  The pins are plain functions so
+that the mutation tests can run all of them against a deliberately broken
+oracle and see at least one fail.
+"""
+from __future__ import annotations
+
+import math
+import os
+from dataclasses import replace
+
+import numpy as np
+import scipy.special
+import torch
+
+from oracle import dsv4_oracle as O
+from hybrid_sparse_mqa_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- helpers
+def _golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            k, v = line.split("=", 1)
+            vals[k.strip()] = [int(x) for x in v.split()]
+    return vals
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    err = np.max(np.abs(a - b)) if a.size else 0.0
+    scale = max(1.0, float(np.max(np.abs(b))) if b.size else 1.0)
+    assert err <= tol * scale, f"{what}: max err {err:.3e} > {tol:.1e}"
+
+
+def _torch_bf16_to_f64(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def _torch_fp8_rows_to_f64(raw):
+    """Library decode of packed rows: torch's float8_e4m3fn widening for the
+    codes, numpy byte views for the scales and rope."""
+    raw = np.ascontiguousarray(raw)
+    n = raw.shape[0]
+    codes = torch.from_numpy(raw[:, :448].copy()).view(torch.float8_e4m3fn).double().numpy()
+    scales = raw[:, 576:604].copy().view("<f4").astype(np.float64)
+    nope = codes * np.repeat(scales, 64, axis=1)
+    rope = _torch_bf16_to_f64(raw[:, 448:576].copy().view("<u2"))
+    return np.concatenate([nope, rope], axis=1).reshape(n, 512)
+
+
+def small_inputs(kind, *, kv_format="bf16", qlen=1, seed=0, heads=2, seq_lens=None):
+    """Tiny inputs that still cross a page boundary and the window edge."""
+    base = dict(swa=0, c4=4, c128=128)[kind]
+    if seq_lens is None:
+        seq_lens = dict(swa=(300, 7, 257), c4=(700, 515, 90), c128=(640, 255, 129))[kind]
+    return synth.make_inputs(
+        synth.Workload(f"pin_{kind}", batch=len(seq_lens), heads=heads, ratio=base,
+                       seq_lens=tuple(seq_lens), qlen=qlen, topk=16, kv_format=kv_format,
+                       decoy_pages=2, seed=seed),
+        device="cpu")
+
+
+def run_oracle(inp, **kw):
+    args = inp.oracle_kwargs()
+    args.update(kw)
+    return O.dsv4_attention(**args)
+
+
+# ------------------------------------------------------- brute force
+def brute_force_token(inp, t, heads=None):
+    """Dense attention over the request's whole logical history with an
+    explicit boolean mask, in pure Python floats.  Independent of the oracle:
+    coordinates are re-derived, pages are walked forwards (physical page ->
+    logical rows), stored values are widened by torch."""
+    kw = inp.oracle_kwargs()
+    seq = [int(x) for x in kw["seq_lens"]]
+    cu = kw["cu_seqlens_q"]
+    # request and position of token t
+    if cu is None:
+        b, p = t, seq[t] - 1
+    else:
+        b = max(i for i in range(len(seq)) if int(cu[i]) <= t)
+        qlen = int(cu[b + 1]) - int(cu[b])
+        p = seq[b] - qlen + (t - int(cu[b]))
+    row = b if kw["req_pool_indices"] is None else int(kw["req_pool_indices"][b])
+    ratio, window = kw["compress_ratio"], kw["window"]
+
+    def widen(pool, rows):
+        if kw["kv_format"] == "bf16":
+            return _torch_bf16_to_f64(pool[rows])
+        return _torch_fp8_rows_to_f64(pool[rows])
+
+    def forward_map(table):
+        m = {}
+        for lp, page in enumerate(table[row]):
+            if page >= 0:
+                for off in range(256):
+                    m[lp * 256 + off] = int(page) * 256 + off
+        return m
+
+    keys, mask = [], []
+    swa_map = forward_map(kw["swa_page_table"])
+    for j in range(0, p + 1):
+        keys.append(("swa", swa_map[j]) if (p - j) < window else None)
+        mask.append((p - j) < window)
+    if ratio:
+        ex_map = forward_map(kw["extra_page_table"])
+        n_total = seq[b] // ratio
+        chosen = None
+        if ratio == 4:
+            chosen = {int(x) for x in kw["topk_idx"][t] if int(x) >= 0}
+        for i in range(n_total):
+            visible = (i + 1) * ratio <= p + 1
+            on = visible and (chosen is None or i in chosen)
+            keys.append(("ex", ex_map[i]) if on else None)
+            mask.append(on)
+    vals = []
+    for k, on in zip(keys, mask):
+        if not on:
+            continue
+        pool = kw["swa_pool"] if k[0] == "swa" else kw["extra_pool"]
+        vals.append(widen(pool, [k[1]])[0].tolist())
+    qv = _torch_bf16_to_f64(kw["q_bits"][t])
+    H = qv.shape[0]
+    heads = range(H) if heads is None else heads
+    scale = kw["scale"]
+    sink = [float(np.float32(x)) for x in kw["sink"]]
+    out, lse = {}, {}
+    for h in heads:
+        qh = qv[h].tolist()
+        logits = [scale * sum(a * c for a, c in zip(qh, v)) for v in vals]
+        mx = max(logits + [sink[h]])
+        w = [math.exp(x - mx) for x in logits]
+        den = sum(w) + math.exp(sink[h] - mx)
+        out[h] = [sum(w[j] * vals[j][d] for j in range(len(vals))) / den for d in range(512)]
+        lse[h] = mx + math.log(den)
+    return out, lse, len(vals)
+
+
+# ------------------------------------------------------------ pins
+def pin_e4m3_spec():
+    v = O.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    assert v[0x00] == 0.0 and v[0x80] == 0.0 and math.copysign(1, v[0x80]) < 0
+    assert v[0x01] == 2.0 ** -9 and v[0x07] == 7 * 2.0 ** -9
+    assert v[0x08] == 2.0 ** -6
+    assert v[0x38] == 1.0 and v[0x3C] == 1.5 and v[0xB8] == -1.0
+    assert v[0x7E] == 448.0 and v[0xFE] == -448.0
+    assert math.isnan(v[0x7F]) and math.isnan(v[0xFF])
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(v))
+    assert np.array_equal(ref[~nan], v[~nan])
+
+
+def pin_bf16_exact():
+    rng = np.random.default_rng(1)
+    bits = rng.integers(0, 1 << 16, size=4096, dtype=np.uint32).astype(np.uint16)
+    bits = bits[((bits >> 7) & 0xFF) != 0xFF]          # drop inf / NaN patterns
+    assert np.array_equal(O.bf16_bits_to_f64(bits), _torch_bf16_to_f64(bits))
+
+
+def pin_fp8_unpack_closed_form():
+    raw = np.zeros((1, 608), dtype=np.uint8)
+    raw[0, :448] = 0x38                                   # e4m3 1.0
+    raw[0, 576:604] = np.arange(1, 8, dtype="<f4").view(np.uint8)
+    raw[0, 448:576] = np.full(64, 0xBF80, dtype="<u2").view(np.uint8)   # bf16 -1.0
+    got = O.unpack_fp8_rows(raw)[0]
+    want = np.concatenate([np.repeat(np.arange(1, 8, dtype=np.float64), 64), -np.ones(64)])
+    assert np.array_equal(got, want)
+
+
+def pin_fp8_unpack_roundtrip():
+    g = torch.Generator().manual_seed(3)
+    x = (torch.randn(64, 512, generator=g) * 0.5).to(torch.bfloat16)
+    raw = synth.pack_fp8_rows(x).numpy()
+    got = O.unpack_fp8_rows(raw)
+    xf = x.double().numpy()
+    scales = raw[:, 576:604].copy().view("<f4").astype(np.float64)
+    step = np.repeat(scales, 64, axis=1)
+    err = np.abs(got[:, :448] - xf[:, :448])
+    # e4m3 keeps 3 mantissa bits: relative error <= 2^-4 for normals, absolute
+    # error <= half the subnormal step 2^-10 * scale below the normal range
+    assert np.all(err <= np.abs(xf[:, :448]) * 2.0 ** -4 + step * 2.0 ** -10 + 1e-300)
+    assert np.array_equal(got[:, 448:], xf[:, 448:])
+    assert np.array_equal(got, _torch_fp8_rows_to_f64(raw))
+
+
+def pin_token_coordinates_golden():
+    g = _golden("request_mapping.txt")
+    req, pos = O.token_coordinates(g["decode.seq_lens"])
+    assert pos.tolist() == g["decode.positions"] and req.tolist() == g["decode.requests"]
+    req, pos = O.token_coordinates(g["decode.seq_lens"], g["decode.cu_seqlens_q"])
+    assert pos.tolist() == g["decode.positions"] and req.tolist() == g["decode.requests"]
+    cu = np.concatenate([[0], np.cumsum(g["prefill.extend_lens"])]).tolist()
+    assert cu == g["prefill.cu_seqlens_q"]
+    req, pos = O.token_coordinates(g["prefill.seq_lens"], cu)
+    assert pos.tolist() == g["prefill.positions"] and req.tolist() == g["prefill.requests"]
+
+
+def pin_req_pool_indices_golden():
+    g = _golden("request_mapping.txt")
+    inp = synth.make_inputs("swa_tiny")            # req_pool_indices = (5, 9)
+    assert inp.req_pool_indices.tolist() == g["req_pool_indices"]
+    res = run_oracle(inp)
+    table = inp.swa_page_table.numpy()
+    for b, r in enumerate(g["req_pool_indices"]):
+        want = [int(table[r, 0]) * 256 + j for j in range(g["decode.positions"][b] + 1)]
+        assert res.rows[b] == want, (b, res.rows[b][:4], want[:4])
+
+
+def pin_softmax_without_sink():
+    rng = np.random.default_rng(2)
+    q, k = rng.standard_normal((4, 512)), rng.standard_normal((37, 512))
+    out, lse = O.attend(q, k, np.full(4, -np.inf), 0.044)
+    s = 0.044 * q @ k.T
+    _close(out, scipy.special.softmax(s, axis=1) @ k, 1e-12, "softmax")
+    _close(lse, scipy.special.logsumexp(s, axis=1), 1e-12, "logsumexp")
+    out2, _ = O.attend(q, k, np.full(4, -1e30), 0.044)     # the pages' no-op sink value
+    _close(out2, out, 1e-12, "sink -1e30")
+
+
+def pin_identical_keys_closed_form():
+    rng = np.random.default_rng(3)
+    q, k = rng.standard_normal((3, 512)), rng.standard_normal(512)
+    sink = np.array([0.0, 1.5, -2.0])
+    for n in (1, 5, 130):
+        out, lse = O.attend(q, np.tile(k, (n, 1)), sink, 0.05)
+        s = 0.05 * q @ k
+        den = n * np.exp(s) + np.exp(sink)
+        _close(out, (n * np.exp(s) / den)[:, None] * k[None, :], 1e-12, f"identical n={n}")
+        _close(lse, np.log(den), 1e-12, f"identical lse n={n}")
+
+
+def pin_attend_brute_force():
+    rng = np.random.default_rng(4)
+    q, k = rng.standard_normal((3, 8)), rng.standard_normal((5, 8))
+    sink = np.array([0.3, -1.0, 2.0])
+    out, lse = O.attend(q, k, sink, 0.7)
+    for h in range(3):
+        e = [math.exp(0.7 * sum(q[h, d] * k[j, d] for d in range(8))) for j in range(5)]
+        den = sum(e) + math.exp(sink[h])
+        for d in range(8):
+            assert abs(out[h, d] - sum(e[j] * k[j, d] for j in range(5)) / den) < 1e-12
+        assert abs(lse[h] - math.log(den)) < 1e-12
+    out0, lse0 = O.attend(q, np.zeros((0, 8)), sink, 0.7)   # no keys: only the sink
+    assert np.all(out0 == 0) and np.array_equal(lse0, sink)
+
+
+def _pin_step_brute(kind, kv_format, qlen, tokens):
+    inp = small_inputs(kind, kv_format=kv_format, qlen=qlen)
+    res = run_oracle(inp)
+    assert res.errors == 0
+    for t in tokens:
+        out, lse, n = brute_force_token(inp, t)
+        assert n == sum(1 for r in res.rows[t] if r >= 0)
+        for h in out:
+            _close(res.out[t, h], out[h], 1e-10, f"{kind} t={t} h={h}")
+            assert abs(res.lse[t, h] - lse[h]) < 1e-10
+
+
+def pin_swa_brute():
+    _pin_step_brute("swa", "bf16", 1, [0, 1, 2])
+
+
+def pin_c4_brute():
+    _pin_step_brute("c4", "bf16", 1, [0, 1, 2])
+
+
+def pin_c128_brute():
+    _pin_step_brute("c128", "bf16", 1, [0, 1, 2])
+
+
+def pin_verify_brute():
+    _pin_step_brute("c4", "bf16", 3, [0, 2, 4, 8])
+    _pin_step_brute("c128", "bf16", 2, [0, 1, 3, 5])
+
+
+def pin_fp8_brute():
+    _pin_step_brute("c4", "fp8", 2, [0, 3])
+    _pin_step_brute("swa", "fp8", 1, [2])
+
+
+def pin_index_permutation_invariance():
+    inp = small_inputs("c4", seed=5)
+    base = run_oracle(inp)
+    g = torch.Generator().manual_seed(6)
+    perm = torch.stack([r[torch.randperm(r.shape[0], generator=g)] for r in inp.topk_idx])
+    inp2 = replace(inp, topk_idx=perm)
+    _close(run_oracle(inp2).out, base.out, 1e-12, "index permutation")
+
+
+def pin_page_permutation_invariance():
+    for kind in ("swa", "c4"):
+        inp = small_inputs(kind, seed=7)
+        base = run_oracle(inp)
+        g = torch.Generator().manual_seed(8)
+
+        def relabel(pool, table):
+            n = pool.shape[0] // 256
+            perm = torch.randperm(n, generator=g)            # old page -> new page
+            newpool = torch.empty_like(pool)
+            newpool.view(n, 256, -1)[perm] = pool.view(n, 256, -1)
+            t = table.clone()
+            t[t >= 0] = perm[t[t >= 0].long()].to(torch.int32)
+            return newpool, t
+        sp, st = relabel(inp.swa_pool, inp.swa_page_table)
+        kw = dict(swa_pool=sp, swa_page_table=st)
+        if inp.extra_pool is not None:
+            ep, et = relabel(inp.extra_pool, inp.extra_page_table)
+            kw.update(extra_pool=ep, extra_page_table=et)
+        res = run_oracle(replace(inp, **kw))
+        assert np.array_equal(res.out, base.out), kind
+
+
+def pin_verify_causality():
+    inp = small_inputs("c128", qlen=3, seed=9, seq_lens=(400, 260))
+    base = run_oracle(inp)
+    # request 0's query rows sit at positions 397, 398, 399: overwrite the
+    # window row of position 399 and check token 0 and 1 do not move
+    table = inp.swa_page_table
+    pool = inp.swa_pool.clone()
+    prow = int(table[0, 399 // 256]) * 256 + 399 % 256
+    pool[prow] = (pool[prow].float() + 3.0).to(pool.dtype)
+    res = run_oracle(replace(inp, swa_pool=pool))
+    assert np.array_equal(res.out[:2], base.out[:2])
+    assert not np.allclose(res.out[2], base.out[2])
+
+
+def pin_c4_all_rows_equals_dense():
+    # request lengths <= 4 * 16 rows so n_c(p) <= topk for ratio 4
+    inp = small_inputs("c4", seq_lens=(60, 33), seed=10)
+    idx = torch.full_like(inp.topk_idx, -1)
+    for t in range(inp.T):
+        n_c = int(inp.seq_lens[t]) // 4
+        idx[t, :n_c] = torch.arange(n_c, dtype=torch.int32)
+    c4 = run_oracle(replace(inp, topk_idx=idx))
+    # dense attention over the window rows followed by every compressed row
+    kw = inp.oracle_kwargs()
+    table = kw["extra_page_table"]
+    for t in range(inp.T):
+        p = int(inp.seq_lens[t]) - 1
+        rows = [int(table[t, i // 256]) * 256 + i % 256 for i in range((p + 1) // 4)]
+        win = c4.rows[t][: min(p + 1, 128)]
+        keys = np.concatenate([O.bf16_bits_to_f64(kw["swa_pool"][win]),
+                               O.bf16_bits_to_f64(kw["extra_pool"][rows])])
+        out, lse = O.attend(O.bf16_bits_to_f64(kw["q_bits"][t]), keys,
+                            kw["sink"].astype(np.float64), kw["scale"])
+        _close(c4.out[t], out, 1e-12, "c4 all rows")
+        _close(c4.lse[t], lse, 1e-12, "c4 all rows lse")
+
+
+def pin_error_reporting():
+    inp = small_inputs("c4", seed=11)
+    t = inp.swa_page_table.clone()
+    t[0, 699 // 256] = inp.swa_pool.shape[0] // 256          # page id past the pool
+    idx = inp.topk_idx.clone()
+    idx[1, 0] = (515 // 4)                                    # n_c(514) = 128: out of range
+    idx[1, 1] = -1                                            # absent: not an error
+    res = run_oracle(replace(inp, swa_page_table=t, topk_idx=idx))
+    assert res.errors == (O.ERR_SWA_PAGE | O.ERR_INDEX_RANGE)
+    assert res.rows[1][min(515, 128)] == -1 and res.rows[1][min(515, 128) + 1] == -1
+    ok = run_oracle(inp)
+    assert ok.errors == 0
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,120 @@
+"""The oracle against its pins, and the pins against plausible oracle mistakes."""
+import numpy as np
+import pytest
+
+from oracle import dsv4_oracle as O
+from tests import _pins
+
+
+@pytest.mark.parametrize("pin", _pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin()
+
+
+# Each mutant is a plausible mistake in the oracle; at least one pin must fail.
+def _m_window_short(pos, window):
+    return list(range(max(0, pos - window + 2), pos + 1))
+
+
+def _m_window_excludes_self(pos, window):
+    return list(range(max(0, pos - window), pos))
+
+
+def _m_visible_floor(pos, ratio):
+    return pos // ratio
+
+
+def _m_sink_scaled(q, keys, sink, scale):
+    return _ATTEND(q, keys, np.asarray(sink, dtype=np.float64) * scale, scale)
+
+
+def _m_sink_dropped(q, keys, sink, scale):
+    out, lse = _ATTEND(q, keys, np.full(np.shape(sink), -np.inf), scale)
+    return out, lse
+
+
+def _m_lse_without_sink(q, keys, sink, scale):
+    out, _ = _ATTEND(q, keys, sink, scale)
+    _, lse = _ATTEND(q, keys, np.full(np.shape(sink), -np.inf), scale)
+    return out, lse
+
+
+def _m_value_without_rope(q, keys, sink, scale):
+    out, lse = _ATTEND(q, keys, sink, scale)
+    k = np.array(keys, dtype=np.float64).reshape(-1, np.shape(q)[1])
+    if k.shape[0]:
+        k[:, 448:] = 0.0
+        s = scale * (np.asarray(q) @ np.asarray(keys).reshape(-1, np.shape(q)[1]).T)
+        m = np.maximum(s.max(axis=1), sink)
+        e = np.exp(s - m[:, None])
+        out = (e @ k) / (np.exp(np.asarray(sink) - m) + e.sum(axis=1))[:, None]
+    return out, lse
+
+
+def _m_e4m3_bias8(codes):
+    return _E4M3(codes) * 0.5
+
+
+def _m_scale_index_mod(raw):
+    raw = np.ascontiguousarray(np.asarray(raw, dtype=np.uint8))
+    n = raw.shape[0]
+    nope = O.e4m3_to_f64(raw[:, :448])
+    sc = raw[:, 576:604].copy().view("<f4").astype(np.float64).reshape(n, 7)
+    nope = nope * sc[:, np.arange(448) % 7]
+    rope = O.bf16_bits_to_f64(raw[:, 448:576].copy().view("<u2"))
+    return np.concatenate([nope, rope], axis=1)
+
+
+def _m_page_offset(page_table, req_row, logical, num_pages):
+    lp = logical // 256
+    if lp < 0 or lp >= page_table.shape[1]:
+        return -1
+    page = int(page_table[req_row, lp])
+    if page < 0 or page >= num_pages:
+        return -1
+    return page * 256 + lp
+
+
+def _m_verify_shift(seq_lens, cu_seqlens_q=None):
+    req, pos = _COORD(seq_lens, cu_seqlens_q)
+    if cu_seqlens_q is not None:
+        pos = pos + 1
+    return req, pos
+
+
+def _m_decode_shift(seq_lens, cu_seqlens_q=None):
+    req, pos = _COORD(seq_lens, cu_seqlens_q)
+    return req, (pos + 1 if cu_seqlens_q is None else pos)
+
+
+_ATTEND = O.attend
+_E4M3 = O.e4m3_to_f64
+_COORD = O.token_coordinates
+
+MUTANTS = {
+    "window_short": ("swa_positions", _m_window_short),
+    "window_excludes_self": ("swa_positions", _m_window_excludes_self),
+    "visible_floor": ("visible_compressed", _m_visible_floor),
+    "sink_scaled": ("attend", _m_sink_scaled),
+    "sink_dropped": ("attend", _m_sink_dropped),
+    "lse_without_sink": ("attend", _m_lse_without_sink),
+    "value_without_rope": ("attend", _m_value_without_rope),
+    "e4m3_bias8": ("e4m3_to_f64", _m_e4m3_bias8),
+    "scale_index_mod": ("unpack_fp8_rows", _m_scale_index_mod),
+    "page_offset": ("physical_row", _m_page_offset),
+    "verify_shift": ("token_coordinates", _m_verify_shift),
+    "decode_shift": ("token_coordinates", _m_decode_shift),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(O, attr, fn)
+    caught = []
+    for pin in _pins.ALL_PINS:
+        try:
+            pin()
+        except (AssertionError, KeyError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
