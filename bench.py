@@ -1,0 +1,446 @@
+"""Benchmark of the hybrid sparse MQA attention step on GB300.
+
+One step = one call of the attention step over one batch of the workload
+(key-slot resolution, gather, QK^T, sink softmax, PV, split merge, write).
+Default workload: C4 top-512 decode, batch 32, H=64, D=512 bf16, context
+65536 (16384 compressed rows per request) + SWA window 128.
+
+Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own replica of the workload
+(requests are independent; there is no collective on the data path); the
+timed region is bracketed by barriers and the slowest rank's time is used.
+
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "query-tokens/s and achieved HBM GB/s (% roofline) for C4 top-512 sparse MQA decode"
+DEFAULT_WORKLOAD = "c4_decode"
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d.get("hbm_gbs"), bf16_tflops=d.get("bf16_tflops"),
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in ("hybrid_sparse_mqa_gb300/csrc/dsv4_attn.cu", "hybrid_sparse_mqa_gb300/csrc/dsv4_device.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per launch of the main kernel from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dsv4_attn_kernel_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    ent = d.get(workload)
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        t0, t1 = (self.marks + [0, 0])[:2] if len(self.marks) >= 2 else (0, 1e30)
+        inside = [l for (t, l) in self.lines if t0 - 0.25 <= t <= t1 + 0.25] or [l for _, l in self.lines]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in inside:
+            parts = [x.strip() for x in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_bytes_and_flops(inp):
+    """Bytes one call must move at minimum and the FLOPs it must do.
+
+    Bytes: q + every distinct KV row attended (row_bytes each) + the C4 index
+    lists + the page-table entries the resolution reads (one per distinct
+    page touched per request) + seq_lens (+ cu_seqlens_q) + out + lse.
+    FLOPs: 4*H*512 per (token, attended key): QK^T and PV, 2 each per MAC.
+    """
+    seq = inp.seq_lens.cpu().tolist()
+    if inp.cu_seqlens_q is None:
+        reqs = list(range(len(seq)))
+        poss = [s - 1 for s in seq]
+    else:
+        cu = inp.cu_seqlens_q.cpu().tolist()
+        reqs = [b for b in range(len(seq)) for _ in range(cu[b + 1] - cu[b])]
+        poss = [seq[b] - (cu[b + 1] - cu[b]) + i for b in range(len(seq)) for i in range(cu[b + 1] - cu[b])]
+    topk = None if inp.topk_idx is None else inp.topk_idx.cpu().tolist()
+    T, H = inp.T, inp.H
+    w = inp.work
+    row_b = 1024 if w.kv_format == "bf16" else 604
+    swa_rows, ex_rows, pages = set(), set(), set()
+    keys = 0
+    for t in range(T):
+        b, p = int(reqs[t]), int(poss[t])
+        first = max(0, p - w.window + 1)
+        for j in range(first, p + 1):
+            swa_rows.add((b, j))
+            pages.add(("s", b, j // 256))
+        n_sw = p + 1 - first
+        if w.ratio == 4:
+            idx = [int(x) for x in topk[t] if x >= 0]
+        elif w.ratio == 128:
+            idx = list(range((p + 1) // 128))
+        else:
+            idx = []
+        for i in idx:
+            ex_rows.add((b, i))
+            pages.add(("e", b, i // 256))
+        keys += n_sw + len(idx)
+    nbytes = (T * H * 512 * 2 * 2 + T * H * 4 + (len(swa_rows) + len(ex_rows)) * row_b + 4 * len(pages)
+              + 4 * w.batch + (0 if inp.topk_idx is None else inp.topk_idx.numel() * 4)
+              + (0 if inp.cu_seqlens_q is None else 4 * (w.batch + 1)))
+    flops = 4.0 * H * 512 * keys
+    return nbytes, flops
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+def run_reference(args):
+    import numpy as np
+    import torch
+    from hybrid_sparse_mqa_gb300 import synth
+    from oracle import dsv4_oracle as O
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    inp = synth.make_inputs(args.workload, device="cpu")
+    kw = inp.oracle_kwargs()
+    T = inp.T
+    per_step_tokens = min(T, args.ref_tokens)
+    # one warm-up token, then W + K bounded steps over `per_step_tokens` tokens each
+    O.dsv4_attention(**kw, tokens=[0])
+    for w in range(args.warmup):
+        O.dsv4_attention(**kw, tokens=list(range(min(per_step_tokens, T))))
+    t0 = time.perf_counter()
+    done = 0
+    for k in range(args.steps):
+        toks = [(k * per_step_tokens + i) % T for i in range(per_step_tokens)]
+        O.dsv4_attention(**kw, tokens=toks)
+        done += len(toks)
+    dt = time.perf_counter() - t0
+    value = done / dt
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "query-tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "tokens_per_step": per_step_tokens,
+                   "note": f"oracle sample: {per_step_tokens} of the {T} query tokens per step"},
+        "cpu_baseline": {"value": value, "unit": "query-tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} steps x {per_step_tokens} tokens of {args.workload}"},
+        "e2e": {"value": value, "unit": "query-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from hybrid_sparse_mqa_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    from hybrid_sparse_mqa_gb300 import attn, synth
+
+    # ---- rotating input sets, each with its own pools: the data one step
+    # reads was last touched R steps earlier, so it is not in L2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sets = []
+    for r in range(args.sets):
+        sets.append(synth.make_inputs(args.workload, device=dev, seed=1000 * (rank + 1) + r))
+    inp0 = sets[0]
+    T, H = inp0.T, inp0.H
+    nbytes, flops = algorithmic_bytes_and_flops(inp0)
+    outs = [torch.empty_like(s.q) for s in sets]
+    lses = [torch.empty(T, H, dtype=torch.float32, device=dev) for _ in sets]
+    w = inp0.work
+    sc, sg = attn.dsv4_attn_plan(T, H, w.ratio, w.window, w.topk if w.ratio == 4 else 0, inp0.max_seq_len, 0)
+    wsz = attn.dsv4_attn_workspace_size(T, H, w.ratio, w.window, w.topk if w.ratio == 4 else 0,
+                                        inp0.max_seq_len, 0)
+    ws = torch.empty(max(wsz, 1), dtype=torch.uint8, device=dev)
+    launches_per_step = 1 + (1 if sg > 1 else 0)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(k, s=stream):
+        i = k % len(sets)
+        attn.run_inputs(sets[i], out=outs[i], lse=lses[i], workspace=ws, stream=s)
+
+    # ---- warm-up (also warms the library's per-device cache before capture)
+    with torch.cuda.stream(stream):
+        for k in range(max(args.warmup, 1)):
+            step(k)
+    torch.cuda.synchronize()
+    if attn.dsv4_attn_get_device_error(stream) != 0:
+        raise RuntimeError("device error flags set during warm-up")
+
+    # ---- one CUDA graph holds one call per input set; replays cover K steps
+    R = len(sets)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for k in range(R):
+            step(k, torch.cuda.current_stream())
+    full, rem = divmod(args.steps, R)
+    tail = None
+    if rem:
+        tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tail, stream=stream):
+            for k in range(rem):
+                step(k, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    # spin the GPU for a moment so the clock samples see it under load
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, int(0.5 / max(1e-6, 6e-6 * R)))):
+            graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(full):
+            graph.replay()
+        if tail is not None:
+            tail.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks.mark()
+    clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = tt.item()
+    flags = attn.dsv4_attn_get_device_error(stream)
+    sec_per_step = ms / 1e3 / args.steps
+    value = world * T / sec_per_step
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda x: x.cpu().pin_memory()
+    hq = [pin(s.q) for s in sets]
+    hidx = [pin(s.topk_idx) if s.topk_idx is not None else None for s in sets]
+    hseq = [pin(s.seq_lens) for s in sets]
+    hout = [torch.empty(T, H, 512, dtype=torch.bfloat16).pin_memory() for _ in sets]
+    hlse = [torch.empty(T, H, dtype=torch.float32).pin_memory() for _ in sets]
+    h2d = hq[0].numel() * 2 + hseq[0].numel() * 4 + (0 if hidx[0] is None else hidx[0].numel() * 4)
+    d2h = hout[0].numel() * 2 + hlse[0].numel() * 4
+
+    def e2e_step(k):
+        i = k % R
+        s = sets[i]
+        s.q.copy_(hq[i], non_blocking=True)
+        s.seq_lens.copy_(hseq[i], non_blocking=True)
+        if hidx[i] is not None:
+            s.topk_idx.copy_(hidx[i], non_blocking=True)
+        attn.run_inputs(s, out=outs[i], lse=lses[i], workspace=ws, stream=stream)
+        hout[i].copy_(outs[i], non_blocking=True)
+        hlse[i].copy_(lses[i], non_blocking=True)
+
+    e2e_steps = min(args.steps, args.e2e_steps)
+    with torch.cuda.stream(stream):
+        for k in range(3):
+            e2e_step(k)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for k in range(e2e_steps):
+            e2e_step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ems = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([ems], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ems = tt.item()
+    e2e_value = world * T / (ems / 1e3 / e2e_steps)
+
+    # ---- oracle on the host, bounded sample of the same workload (rank 0, N=1)
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import dsv4_oracle as O
+        kw = sets[0].oracle_kwargs()
+        O.dsv4_attention(**kw, tokens=[0])
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < args.cpu_seconds and n < T * 8:
+            O.dsv4_attention(**kw, tokens=[n % T])
+            n += 1
+        dt = time.perf_counter() - t0
+        cpu_baseline = {"value": n / dt, "unit": "query-tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                        "sample": f"{n} query tokens of {args.workload} one at a time, {dt:.1f} s, numpy "
+                                  f"float64 (BLAS threads = host default)"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    peaks = measured_peaks()
+    per_launch_s = sec_per_step / launches_per_step if launches_per_step == 1 else sec_per_step
+    achieved = nbytes / per_launch_s / 1e9
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "query-tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": sec_per_step * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "batch": w.batch, "heads": H, "head_dim": 512,
+                   "context": int(inp0.max_seq_len), "topk": w.topk if w.ratio == 4 else 0,
+                   "window": w.window, "input_sets": R,
+                   "l2": f"inputs larger than L2: {R} rotating sets with their own pools "
+                         f"({R * nbytes / 1e6:.0f} MB touched per rotation vs L2 {l2 / 1e6:.0f} MB)",
+                   "split_plan": {"cluster_splits": sc, "grid_splits": sg},
+                   "timing": "CUDA graph replays of one call per input set, CUDA events on the launch stream"},
+        "gpu_launches": args.steps * launches_per_step,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(args.workload),
+                     "peak_source": peaks["source"], "algorithmic_bytes_per_launch": nbytes,
+                     "flops_per_launch": flops,
+                     "tensor_frac": flops / per_launch_s / 1e12 / peaks["bf16_tflops"],
+                     "us_per_launch": per_launch_s * 1e6},
+        "e2e": {"value": e2e_value, "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "cpu_baseline": cpu_baseline,
+        "clocks": clocks.summary(),
+        "device_error_flags": flags,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--sets", type=int, default=12)
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-tokens", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,150 @@
+"""CUDA path (through the C ABI) against the float64 oracle.
+
+Tolerances: bf16 inputs ~ N(0,1)*0.5 -> max |out - oracle| <= 1e-2 and mean
+|out - oracle| <= 1e-3; packed FP8 KV -> max <= 3e-2 against the oracle on the
+same dequantised values; lse within 1e-3.  The gathered row sets must match
+the oracle's bit for bit (debug dump).
+"""
+import numpy as np
+import pytest
+import torch
+
+from hybrid_sparse_mqa_gb300 import synth
+from oracle import dsv4_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+TOL_MAX_BF16, TOL_MEAN_BF16, TOL_MAX_FP8, TOL_LSE = 1e-2, 1e-3, 3e-2, 1e-3
+
+
+@pytest.fixture(scope="module")
+def attn():
+    from hybrid_sparse_mqa_gb300 import build
+    build.build()
+    from hybrid_sparse_mqa_gb300 import attn as A
+    A.lib()
+    A.dsv4_attn_get_device_error()     # start from a clean error word
+    return A
+
+
+def run_and_compare(A, inp, *, tokens=None, num_splits=0, check_rows=True):
+    dev = torch.device("cuda")
+    g = inp.to(dev) if inp.q.device.type != "cuda" else inp
+    stride = A.debug_stride_for(g)
+    dbg = torch.full((g.T, stride), -7, dtype=torch.int32, device=dev) if check_rows else None
+    out, lse = A.run_inputs(g, num_splits=num_splits, debug_rows=dbg)
+    torch.cuda.synchronize()
+    flags = A.dsv4_attn_get_device_error()
+    res = O.dsv4_attention(**g.oracle_kwargs(), tokens=tokens)
+    assert res.errors == 0, f"oracle flagged input errors {res.errors}"
+    assert flags == 0, f"device error flags {flags:#x}"
+    toks = list(range(g.T)) if tokens is None else list(tokens)
+    o = out.float().cpu().numpy()[toks]
+    ref = res.out[toks]
+    assert np.all(np.isfinite(o))
+    err = np.abs(o - ref)
+    fp8 = g.work.kv_format == "fp8"
+    assert err.max() <= (TOL_MAX_FP8 if fp8 else TOL_MAX_BF16), f"max abs err {err.max():.3e}"
+    if not fp8:
+        assert err.mean() <= TOL_MEAN_BF16, f"mean abs err {err.mean():.3e}"
+    lerr = np.abs(lse.cpu().numpy()[toks] - res.lse[toks])
+    assert lerr.max() <= TOL_LSE, f"lse err {lerr.max():.3e}"
+    if check_rows:
+        rows = dbg.cpu().numpy()
+        for t in toks:
+            want = np.full(stride, -1, dtype=np.int64)
+            want[:len(res.rows[t])] = res.rows[t]
+            assert np.array_equal(rows[t], want), f"token {t}: gathered rows differ"
+    return out, lse, float(err.max())
+
+
+def small(kind, heads, seq_lens, *, qlen=1, topk=512, kv_format="bf16", seed=0, rpi=None, sink=None):
+    ratio = dict(swa=0, c4=4, c128=128)[kind]
+    inp = synth.make_inputs(
+        synth.Workload(f"t_{kind}", batch=len(seq_lens), heads=heads, ratio=ratio,
+                       seq_lens=tuple(seq_lens), qlen=qlen, topk=topk, kv_format=kv_format,
+                       req_pool_indices=rpi, seed=seed), device="cuda")
+    if sink is not None:
+        inp.sink.fill_(sink)
+    return inp
+
+
+def test_swa_tiny_all_tokens(attn):
+    inp = synth.make_inputs("swa_tiny", device="cuda")
+    run_and_compare(attn, inp)
+
+
+@pytest.mark.parametrize("heads", [8, 16, 32, 64, 128])
+def test_swa_decode_boundaries(attn, heads):
+    # window edge (128), page edge (255/256/257), single token, multi-page windows
+    run_and_compare(attn, small("swa", heads, (1, 7, 127, 128, 129, 255, 256, 257, 300, 1000), seed=heads))
+
+
+@pytest.mark.parametrize("heads", [16, 64, 128])
+def test_c4_decode_small(attn, heads):
+    # n_c(p) below and above topk (short lists are padded with -1 slots)
+    run_and_compare(attn, small("c4", heads, (4, 100, 515, 2048, 2049, 9000), seed=10 + heads))
+
+
+@pytest.mark.parametrize("topk", [16, 100, 512])
+def test_c4_topk_sizes(attn, topk):
+    run_and_compare(attn, small("c4", 64, (3000, 700, 5000), topk=topk, seed=topk))
+
+
+@pytest.mark.parametrize("heads", [64, 128])
+def test_c128_decode_small(attn, heads):
+    run_and_compare(attn, small("c128", heads, (127, 128, 129, 640, 20000, 70000), seed=20 + heads))
+
+
+@pytest.mark.parametrize("kind", ["swa", "c4", "c128"])
+def test_verify_small(attn, kind):
+    run_and_compare(attn, small(kind, 64, (300, 1029, 5000), qlen=3, seed=30))
+
+
+def test_req_pool_indices(attn):
+    inp = small("c4", 32, (900, 3000), rpi=(5, 9), seed=40)
+    run_and_compare(attn, inp)
+
+
+@pytest.mark.parametrize("sink", [float("-inf"), 0.0, 30.0])
+def test_sink_values(attn, sink):
+    run_and_compare(attn, small("c4", 64, (600, 4000), sink=sink, seed=50))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 4, 7, 8, 12])
+def test_split_invariance(attn, splits):
+    inp = small("c128", 64, (33000, 60000, 129), seed=60)
+    out, _, _ = run_and_compare(attn, inp, num_splits=splits)
+    ref, _, _ = run_and_compare(attn, inp, num_splits=1, check_rows=False)
+    assert (out.float() - ref.float()).abs().max().item() <= 1e-2
+
+
+def test_device_errors_are_flagged_not_trapped(attn):
+    inp = small("c4", 64, (900, 3000, 5000), seed=70)
+    bad_pt = inp.swa_page_table.clone()
+    bad_pt[0, 899 // 256] = inp.swa_pool.shape[0] // 256        # page id past the pool
+    idx = inp.topk_idx.clone()
+    idx[1, 0] = 3000 // 4                                       # >= n_c(2999) = 750
+    from dataclasses import replace
+    bad = replace(inp, swa_page_table=bad_pt, topk_idx=idx)
+    out, lse = attn.run_inputs(bad)
+    torch.cuda.synchronize()
+    flags = attn.dsv4_attn_get_device_error()
+    assert flags & attn.DEV_ERR["SWA_PAGE"] and flags & attn.DEV_ERR["INDEX_RANGE"]
+    assert attn.dsv4_attn_get_device_error() == 0               # read clears
+    res = O.dsv4_attention(**bad.oracle_kwargs())
+    assert res.errors == (O.ERR_SWA_PAGE | O.ERR_INDEX_RANGE)
+    # skipped slots are skipped identically on both sides
+    err = np.abs(out.float().cpu().numpy() - res.out).max()
+    assert err <= TOL_MAX_BF16
+
+
+# ---------------------------------------------------------------- full-size workloads
+@pytest.mark.parametrize("name,tokens", [
+    ("swa_decode", [0, 17, 40, 63]),
+    ("c4_decode", [0, 9, 31]),
+    ("c128_decode", [0, 15]),
+])
+def test_full_size_sampled(attn, name, tokens):
+    inp = synth.make_inputs(name, device="cuda")
+    run_and_compare(attn, inp, tokens=tokens)
