@@ -287,13 +287,14 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.5)
-    # spin the GPU for a moment so the clock samples see it under load
-    with torch.cuda.stream(stream):
-        for _ in range(max(1, int(0.5 / max(1e-6, 6e-6 * R)))):
-            graph.replay()
-    torch.cuda.synchronize()
+    if not args.quick:
+        clocks.start()
+        time.sleep(0.5)
+        # spin the GPU for a moment so the clock samples see it under load
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, int(0.5 / max(1e-6, 6e-6 * R)))):
+                graph.replay()
+        torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -364,13 +365,13 @@ def run_ours(args):
 
     # ---- oracle on the host, bounded sample of the same workload (rank 0, N=1)
     cpu_baseline = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
         from oracle import dsv4_oracle as O
         kw = sets[0].oracle_kwargs()
         O.dsv4_attention(**kw, tokens=[0])
         t0 = time.perf_counter()
         n = 0
-        while time.perf_counter() - t0 < args.cpu_seconds and n < T * 8:
+        while time.perf_counter() - t0 < args.cpu_seconds and n < T * 10000:
             O.dsv4_attention(**kw, tokens=[n % T])
             n += 1
         dt = time.perf_counter() - t0
@@ -436,6 +437,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="no clock sampling, no CPU baseline (for profiler runs)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -3,25 +3,25 @@
 //
 // What is computed is stated in include/dsv4attn.h.  How:
 //
-// * One thread-block cluster of 2*Sc CTAs handles one query token and one
-//   of Sg slices of its key list; CTA (s, c) of the cluster takes piece s of
-//   that slice and half c (dims c*256 .. c*256+255) of every 512-wide row.
-//   Splitting the row dimension between the two CTAs of a pair keeps the
-//   H x 512 fp32 output accumulator within one SM's tensor memory (256 of
-//   its 512 columns) and halves every CTA's gather.
-// * Per 64-key tile: four loader warps resolve key slots to pool rows (SWA
-//   page table, C4 index list, C128 range) and gather their 512-byte row
-//   halves with 16-byte cp.async into a 128-byte-swizzled shared tile; the
-//   MMA warp computes the partial scores Q[:,half] K[:,half]^T on tcgen05
-//   (heads padded to M=128, fp32 in TMEM); the four softmax warps add the
-//   partner CTA's partial scores (exchanged through distributed shared
-//   memory), run an online softmax in registers (thread h owns head h) and
-//   write bf16 probabilities to shared memory; the MMA warp accumulates
-//   O[:,half] += P V[:,half] (V is the same tile, read MN-major).
-// * Splits are merged with their log-sum-exp weights, the sink's exp(sink)
-//   is added to the denominator once, and the bf16 output is written; merges
-//   inside a cluster go through distributed shared memory, merges across
-//   clusters through the workspace and the combine kernel.
+// * A CTA owns one query token, one group of up to 64 of its heads and one
+//   slice of its key list.  The key list (window slots, then C4 / C128 extra
+//   slots) is cut into Sc x Sg slices: the Sc slices of a token share a
+//   thread-block cluster and merge their partial results inside the kernel
+//   (through L2); Sg groups of clusters merge through the workspace and the
+//   combine kernel.  With H = 128 the two head groups of a slice read the
+//   same rows.
+// * Per 64-key tile: eight loader warps resolve key slots to pool rows (SWA
+//   page table, C4 index list, C128 range), prefetch the rows into L2 as soon
+//   as they are resolved, and gather the 1 KB rows with 16-byte cp.async into
+//   a 128-byte-swizzled shared tile.  The MMA warp computes S = Q K^T on
+//   tcgen05 (M = 64 heads, N = 64 keys, K = 512; fp32 in TMEM).  Thread h of
+//   the four softmax warps owns head h's row of S: online softmax with a
+//   lazily updated running max, bf16 probabilities written as one 128-byte
+//   line.  The MMA warp then accumulates O^T += V^T P^T (M = 128 of the 512
+//   value dims per MMA, N = 64 heads, K = 64 keys) into 4 x 64 TMEM columns;
+//   V is the same shared tile read MN-major (K and V are the same row).
+// * At the end the sink adds exp(sink - M) to each head's denominator, the
+//   slices are merged with log-sum-exp weights and the bf16 output written.
 //
 // Sources (page title, section): "SGLang DeepSeek-V4 Attention Test
 // Capability Matrix" - "Input And Config Coverage", "Reference Implementation
@@ -43,34 +43,36 @@ namespace dsv4 {
 // ------------------------------------------------------------------ shape
 constexpr int kDim = 512;
 constexpr int kPageSize = 256;
-constexpr int kTileN = 64;           // key rows per tile
-constexpr int kStages = 3;           // gather pipeline depth
-constexpr int kM = 128;              // MMA M: heads padded to 128
+constexpr int kTileN = 64;           // keys per tile
+constexpr int kStages = 2;           // gather pipeline depth (64 KB each)
+constexpr int kHG = 64;              // heads per CTA (MMA M of S = Q K^T)
 constexpr int kRing = 512;           // resolved key slots held at a time
 constexpr int kSoftmaxWarps = 4;
-constexpr int kLoadWarps = 4;
+constexpr int kLoadWarps = 8;
+constexpr int kLoadThreads = kLoadWarps * 32;
 constexpr int kMmaWarp = kSoftmaxWarps + kLoadWarps;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
-constexpr int kMaxClusterSplits = 4;
+constexpr int kMaxCluster = 8;
 constexpr float kRescaleLog2 = 8.0f; // lazy rescale threshold (factor 256)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;       // two 64-column score buffers
-constexpr uint32_t kTmemO = 256;     // 256-column output accumulator
+constexpr uint32_t kTmemO = 128;     // O^T: 4 x 64 columns, value dim 128*m + lane
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // ------------------------------------------------------------------ smem
-constexpr int kQBytes = 4 * kM * 128;          // 4 chunks of 64 dims
-constexpr int kStageBytes = 4 * kTileN * 128;  // 4 chunks of 64 dims
-constexpr int kPBytes = kM * 128;              // 64 keys x 128 heads bf16
-constexpr int kXBytes = kM * 64 * 4;           // partner's partial scores
+constexpr int kChunk = 64 * 128;               // 64 rows x 128 B: one 64-dim chunk
+constexpr int kQBytes = 8 * kChunk;            // 64 heads x 512 dims
+constexpr int kStageBytes = 8 * kChunk;        // 64 keys x 512 dims
+constexpr int kPBytes = kHG * 128;             // 64 heads x 64 keys bf16
 constexpr int OFF_Q = 0;
 constexpr int OFF_KV = OFF_Q + kQBytes;
 constexpr int OFF_P = OFF_KV + kStages * kStageBytes;
-constexpr int OFF_X = OFF_P + 2 * kPBytes;
-constexpr int OFF_RING = OFF_X + kXBytes;      // int32 rows; (m, l) pairs after the loop
-constexpr int OFF_MASK = OFF_RING + kRing * 4;
+constexpr int OFF_RING = OFF_P + 2 * kPBytes;  // int32 pool rows of resolved slots
+constexpr int OFF_ML = OFF_RING + kRing * 4;   // float2 (m, l) per head
+constexpr int OFF_W = OFF_ML + kHG * 8;        // float per head: rescale / merge weights
+constexpr int OFF_MASK = OFF_W + kHG * 4;      // 64-bit key validity mask per stage
 constexpr int OFF_BAR = OFF_MASK + kStages * 8;
 enum Bar {
     B_Q_FULL = 0,
@@ -82,23 +84,37 @@ enum Bar {
     B_P_FULL = B_S_FREE + 2,
     B_P_FREE = B_P_FULL + 2,
     B_O_FINAL = B_P_FREE + 2,
-    B_X_FULL,
-    B_X_FREE,
     B_COUNT
 };
 constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;
-constexpr int OFF_MERGE = OFF_KV;              // 128 x 256 fp32, reuses KV + P
-constexpr int kSmemUsed = OFF_MISC + 64;
-constexpr int kSmemAlloc = 232448;             // per-block maximum on sm_100/103
-static_assert(OFF_MERGE + kM * 1024 <= OFF_X, "merge buffer must fit in the KV and P buffers");
-static_assert(kM * 8 <= kRing * 4, "(m, l) pairs must fit in the ring");
-static_assert(kSmemUsed <= kSmemAlloc, "shared memory budget");
+constexpr int OFF_MERGE = OFF_KV;              // [owned dim][64 heads] fp32, reuses the KV stages
+constexpr int kSmemUsed = OFF_MISC + 16;
+constexpr int kSmemAlloc = kSmemUsed + 1024;   // room to align the base to 1024 bytes
+static_assert(OFF_MERGE + kDim * kHG * 4 <= OFF_P, "merge buffer must fit in the KV stages");
+static_assert(kSmemAlloc <= 232448, "shared memory budget");
+static_assert(kRing % kLoadThreads == 0, "ring slots per loader thread");
 
 __device__ unsigned int g_dev_error;
+
+// Optional per-CTA phase timestamps (globaltimer ns), compiled in only with
+// -DDSV4_TRACE; read back with dsv4_attn_trace_read().
+#ifdef DSV4_TRACE
+constexpr int kTraceSlots = 64;
+constexpr int kTraceCtas = 2048;
+__device__ unsigned long long g_trace[kTraceCtas * kTraceSlots];
+__device__ __forceinline__ void trace_mark(int slot) {
+    const int cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    if (cta < kTraceCtas && slot < kTraceSlots) g_trace[cta * kTraceSlots + slot] = globaltimer_ns();
+}
+#define DSV4_TR(slot) trace_mark(slot)
+#else
+#define DSV4_TR(slot) ((void)0)
+#endif
 
 struct Params {
     const __nv_bfloat16* q;
     int T, H, batch;
+    int groups;              // head groups of 64 (1 or 2)
     const int* seq_lens;
     const int* cu_seqlens;   // nullable (decode)
     const int* rpi;          // nullable
@@ -117,12 +133,13 @@ struct Params {
     int topk;
     const float* sink;
     float scale_log2;        // scale * log2(e)
-    int chunk;               // key slots per split (multiple of kTileN)
+    int chunk;               // key slots per slice
     int csplits, gsplits;
     __nv_bfloat16* out;
     float* lse;
-    float* part_o;           // [T, Sg, H, 512] when gsplits > 1
+    float* part_o;           // [T, Sg, H, 512] fp32 when gsplits > 1
     float2* part_ml;         // [T, Sg, H]
+    uint16_t* merge;         // [T, Sg, G, Sc, 512, 64] bf16 when csplits > 1
     int* debug_rows;
     int debug_stride;
 };
@@ -131,10 +148,10 @@ struct TokenInfo {
     int trow, pos, n_swa, n_c, L, slot_begin, slot_end, ntiles;
 };
 
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, bool cluster_scope, int* abort_flag) {
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int* abort_flag) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
+        if (mbar_try(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
             if (globaltimer_ns() - t0 > kTimeoutNs) {
@@ -150,14 +167,10 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, bool clust
 // barriers others wait for), so every role reaches the end of the kernel.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int* abort_flag) {
     if (mbar_try(bar, parity)) return true;
-    return wait_slow(bar, parity, false, abort_flag);
-}
-__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, int* abort_flag) {
-    if (mbar_try_cluster(bar, parity)) return true;
-    return wait_slow(bar, parity, true, abort_flag);
+    return wait_slow(bar, parity, abort_flag);
 }
 
-// Query token t -> request row, position and key-list extent of this split.
+// Query token t -> request row, position and key-list extent of slice `split`.
 __device__ void token_info(const Params& p, int t, int split, TokenInfo& ti, unsigned& err) {
     int b, pos;
     bool ok = true;
@@ -229,10 +242,39 @@ __device__ __forceinline__ int resolve_slot(const Params& p, int t, const TokenI
     return page * kPageSize + (idx % kPageSize);
 }
 
+__device__ __forceinline__ const uint8_t* slot_row_ptr(const Params& p, const TokenInfo& ti, int slot, int row) {
+    return slot < ti.n_swa ? p.swa_rows + (size_t)row * p.swa_row_bytes
+                           : p.ex_rows + (size_t)row * p.ex_row_bytes;
+}
+
 // Byte offset of 16-byte piece `piece` (0..7) of the 128-byte line `line` in
 // a 1024-byte-aligned 128B-swizzled buffer.
 __device__ __forceinline__ uint32_t sw128(uint32_t line, uint32_t piece) {
     return line * 128u + ((piece ^ (line & 7u)) << 4);
+}
+
+// Generic address of the same shared-memory object in CTA `rank` of the cluster.
+template <typename T>
+__device__ __forceinline__ const T* cluster_ptr(const T* local, uint32_t rank) {
+    uint64_t r;
+    asm volatile("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
+    return reinterpret_cast<const T*>(r);
+}
+
+// OR of `pred` over the `count` threads taking part in named barrier `id`.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n"
+        " bar.red.or.pred p, %2, %3, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
 template <int KV_FORMAT>
@@ -246,36 +288,34 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
-    const uint32_t half = rank & 1u;
-    const uint32_t csplit = rank >> 1;
-    const uint32_t peer = rank ^ 1u;
+    const int G = p.groups;
+    const int grp = static_cast<int>(rank) % G;        // head group
+    const int cs = static_cast<int>(rank) / G;         // slice within the cluster
+    const int Sc = p.csplits;
     const int t = blockIdx.y;
     const int gsplit = blockIdx.z;
-    const int split = gsplit * p.csplits + static_cast<int>(csplit);
+    const int split = gsplit * Sc + cs;
+    const int head0 = grp * kHG;
+    const int hcount = min(kHG, p.H - head0);
 
-    const uint32_t sQ = base + OFF_Q, sKV = base + OFF_KV, sP = base + OFF_P, sX = base + OFF_X;
-    const uint32_t sMerge = base + OFF_MERGE;
+    const uint32_t sQ = base + OFF_Q, sKV = base + OFF_KV, sP = base + OFF_P;
     int* ring = reinterpret_cast<int*>(smem + OFF_RING);
-    float2* ml = reinterpret_cast<float2*>(smem + OFF_RING);
-    uint16_t* mask16 = reinterpret_cast<uint16_t*>(smem + OFF_MASK);
+    float2* ml = reinterpret_cast<float2*>(smem + OFF_ML);
+    float* wsm = reinterpret_cast<float*>(smem + OFF_W);
+    uint8_t* mask8 = smem + OFF_MASK;
     const uint32_t bars = base + OFF_BAR;
     auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     int* abort_flag = reinterpret_cast<int*>(smem + OFF_MISC + 4);
-    TokenInfo* tinfo = reinterpret_cast<TokenInfo*>(smem + OFF_MISC + 16);
 
     unsigned err = 0;
-    if ((base - raw_base) + kSmemUsed > static_cast<uint32_t>(kSmemAlloc)) {
-        // Same layout in every CTA of the cluster, so all of them leave here.
-        if (threadIdx.x == 0) atomicOr(&g_dev_error, DSV4_DEV_ERR_TIMEOUT);
-        return;
-    }
+    if (tid == 0) DSV4_TR(0);
 
     // ------------------------------------------------------------ set-up
     if (tid == 0) {
-        mbar_init(bar(B_Q_FULL), kLoadWarps * 32);
+        mbar_init(bar(B_Q_FULL), kSoftmaxWarps * 32);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(B_KV_FULL + s), kLoadWarps * 32);
+            mbar_init(bar(B_KV_FULL + s), kLoadThreads);
             mbar_init(bar(B_KV_EMPTY + s), 1);
             mbar_init(bar(B_MASK_FULL + s), kLoadWarps);
         }
@@ -286,123 +326,137 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             mbar_init(bar(B_P_FREE + s), 1);
         }
         mbar_init(bar(B_O_FINAL), 1);
-        mbar_init(bar(B_X_FULL), kSoftmaxWarps * 32);
-        mbar_init(bar(B_X_FREE), kSoftmaxWarps * 32);
         fence_mbar_init_cluster();
         *abort_flag = 0;
-        TokenInfo ti;
-        token_info(p, t, split, ti, err);
-        *tinfo = ti;
+    }
+    // every thread derives the token's coordinates itself (same addresses; the
+    // loads overlap the barrier set-up); thread 0 reports the errors
+    TokenInfo ti;
+    {
+        unsigned e0 = 0;
+        token_info(p, t, split, ti, e0);
+        if (tid == 0) err |= e0;
     }
     if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    cluster_sync();   // every CTA's barriers are initialised before any remote arrival
     const uint32_t tmem = *tmem_slot;
-    const TokenInfo ti = *tinfo;
     const int ntiles = ti.ntiles;
+    if (tid == 0) DSV4_TR(1);
 
     if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
         // ============================================================ loader
         const int lt = tid - kSoftmaxWarps * 32;
         const int lw = lt >> 5;
-        // debug dump of this split's slots (pair half 0 only)
-        if (p.debug_rows != nullptr && half == 0) {
+        if (p.debug_rows != nullptr && grp == 0) {
             const int d0 = split * p.chunk;
             const int d1 = min(d0 + p.chunk, p.debug_stride);
-            for (int s = d0 + lt; s < d1; s += kLoadWarps * 32) {
+            for (int s = d0 + lt; s < d1; s += kLoadThreads) {
                 const int row = (s < ti.L) ? resolve_slot(p, t, ti, s, err) : -1;
                 p.debug_rows[(size_t)t * p.debug_stride + s] = row;
             }
         }
-        // query rows of this half: 128 heads x 512 bytes, zero-filled past H
-        {
-            const uint8_t* qb = reinterpret_cast<const uint8_t*>(p.q) + ((size_t)t * p.H) * 1024 + half * 512;
-            for (int k = lt; k < kM * 32; k += kLoadWarps * 32) {
-                const int h = k >> 5, piece = k & 31;
-                const uint32_t dst = sQ + (piece >> 3) * (kM * 128) + sw128(h, piece & 7);
-                const bool on = h < p.H && ntiles > 0;
-                cp_async_16(dst, on ? qb + (size_t)h * 1024 + piece * 16 : qb, on ? 16u : 0u);
-            }
-            cp_async_arrive_noinc(bar(B_Q_FULL));
-        }
         int ring_base = -1;
         for (int i = 0; i < ntiles; ++i) {
-            const int stage = i % kStages;
+            const int stage = i & 1;
             if (i >= kStages) {
-                wait_bar(bar(B_KV_EMPTY + stage), ((i / kStages) - 1) & 1, abort_flag);
+                wait_bar(bar(B_KV_EMPTY + stage), ((i >> 1) - 1) & 1, abort_flag);
                 fence_proxy_async();
             }
             const int slot0 = ti.slot_begin + i * kTileN;
             if (ring_base < 0 || slot0 + kTileN > ring_base + kRing) {
-                named_barrier_sync(1, kLoadWarps * 32);
+                named_barrier_sync(1, kLoadThreads);
                 ring_base = slot0;
                 const int lim = min(ring_base + kRing, ti.slot_end);
-#pragma unroll 4
-                for (int s = ring_base + lt; s < ring_base + kRing; s += kLoadWarps * 32)
-                    ring[s - ring_base] = (s < lim) ? resolve_slot(p, t, ti, s, err) : -1;
-                named_barrier_sync(1, kLoadWarps * 32);
+                // kRing / kLoadThreads slots per thread, their dependent loads in
+                // flight together; each resolved row is prefetched into L2
+                constexpr int kPer = kRing / kLoadThreads;
+                int rows[kPer];
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const int sl = ring_base + lt + u * kLoadThreads;
+                    rows[u] = (sl < lim) ? resolve_slot(p, t, ti, sl, err) : -1;
+                }
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const int sl = ring_base + lt + u * kLoadThreads;
+                    ring[sl - ring_base] = rows[u];
+                    if (rows[u] >= 0) prefetch_l2(slot_row_ptr(p, ti, sl, rows[u]), 1024);
+                }
+                named_barrier_sync(1, kLoadThreads);
+                if (lt == 0 && ring_base == ti.slot_begin) DSV4_TR(3);
             }
-            // validity mask of this tile, 16 slots per loader warp
             {
-                const int r = lw * 16 + (lane & 15);
+                // validity of the tile's 64 key slots, 8 per loader warp
+                constexpr int kRowsPerWarp = kTileN / kLoadWarps;
+                const int r = lw * kRowsPerWarp + (lane % kRowsPerWarp);
                 const int slot = slot0 + r;
                 const bool valid = slot < ti.slot_end && ring[slot - ring_base] >= 0;
-                const unsigned bal = __ballot_sync(0xffffffffu, lane < 16 && valid);
-                if (lane == 0) mask16[stage * 4 + lw] = static_cast<uint16_t>(bal & 0xffffu);
+                const unsigned bal = __ballot_sync(0xffffffffu, lane < kRowsPerWarp && valid);
+                if (lane == 0) mask8[stage * kLoadWarps + lw] = static_cast<uint8_t>(bal & 0xffu);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_MASK_FULL + stage));
             }
             const uint32_t dst_stage = sKV + stage * kStageBytes;
 #pragma unroll 4
-            for (int k = 0; k < 16; ++k) {
-                const int r = lw * 16 + k;
+            for (int k = 0; k < kTileN / kLoadWarps; ++k) {
+                const int r = lw * (kTileN / kLoadWarps) + k;
                 const int slot = slot0 + r;
                 const int row = slot < ti.slot_end ? ring[slot - ring_base] : -1;
-                const bool from_swa = slot < ti.n_swa;
-                const uint8_t* pool = from_swa ? p.swa_rows : p.ex_rows;
-                const int rb = from_swa ? p.swa_row_bytes : p.ex_row_bytes;
-                const uint8_t* src = row >= 0 ? pool + (size_t)row * rb + half * 512 + lane * 16 : p.swa_rows;
-                const uint32_t dst = dst_stage + (lane >> 3) * (kTileN * 128) + sw128(r, lane & 7);
-                cp_async_16(dst, src, row >= 0 ? 16u : 0u);
+                const uint8_t* src = row >= 0 ? slot_row_ptr(p, ti, slot, row) : p.swa_rows;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int piece = lane + 32 * h2;       // 16-byte piece of the 1 KB row
+                    const uint32_t dst = dst_stage + (piece >> 3) * kChunk + sw128(r, piece & 7);
+                    cp_async_16(dst, src + (row >= 0 ? piece * 16 : 0), row >= 0 ? 16u : 0u);
+                }
             }
             cp_async_arrive_noinc(bar(B_KV_FULL + stage));
+            if (lt == 0 && i < 8) DSV4_TR(4 + i);
         }
         cp_async_wait_all();
     } else if (warp == kMmaWarp) {
         // ============================================================ MMA issuer
         if (lane == 0 && ntiles > 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(kM, kTileN, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kM, 256, false, true);
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(kHG, kTileN, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kHG, true, false);
             wait_bar(bar(B_Q_FULL), 0, abort_flag);
             fence_proxy_async();
             tc_fence_after();
             auto issue_pv = [&](int j) {
                 const int pb = j & 1;
-                const int stage = j % kStages;
+                const uint32_t stg = sKV + (j & 1) * kStageBytes;
                 wait_bar(bar(B_P_FULL + pb), (j >> 1) & 1, abort_flag);
+                if (j < 8) DSV4_TR(20 + j);
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < kTileN / 16; ++k) {
-                    const uint64_t a = smem_desc_sw128(sP + pb * kPBytes + k * 32, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(sKV + stage * kStageBytes + k * 2048, kTileN * 128, 1024);
-                    mma_bf16_ss(tmem + kTmemO, a, b, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+                for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+                    for (int kk = 0; kk < kTileN / 16; ++kk) {
+                        // A = V^T (dims 128*mt.., keys 16*kk..): MN-major, 64-dim atoms one chunk apart
+                        const uint64_t a = smem_desc_sw128(stg + 2 * mt * kChunk + kk * 2048, kChunk, 1024);
+                        // B = P (heads x keys), K-major
+                        const uint64_t b = smem_desc_sw128(sP + pb * kPBytes + kk * 32, 16, 1024);
+                        mma_bf16_ss(tmem + kTmemO + mt * kHG, a, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
                 mma_commit(bar(B_P_FREE + pb));
-                mma_commit(bar(B_KV_EMPTY + stage));
+                mma_commit(bar(B_KV_EMPTY + (j & 1)));
             };
             for (int i = 0; i < ntiles; ++i) {
-                const int stage = i % kStages;
+                const int stage = i & 1;
                 const int sb = i & 1;
-                wait_bar(bar(B_KV_FULL + stage), (i / kStages) & 1, abort_flag);
+                wait_bar(bar(B_KV_FULL + stage), (i >> 1) & 1, abort_flag);
+                if (i < 8) DSV4_TR(12 + i);
                 fence_proxy_async();
                 if (i >= 2) wait_bar(bar(B_S_FREE + sb), ((i - 2) >> 1) & 1, abort_flag);
                 tc_fence_after();
+                const uint32_t stg = sKV + stage * kStageBytes;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const uint64_t a = smem_desc_sw128(sQ + (k >> 2) * (kM * 128) + (k & 3) * 32, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(sKV + stage * kStageBytes + (k >> 2) * (kTileN * 128) + (k & 3) * 32, 16, 1024);
+                for (int k = 0; k < kDim / 16; ++k) {
+                    const uint64_t a = smem_desc_sw128(sQ + (k >> 2) * kChunk + (k & 3) * 32, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(stg + (k >> 2) * kChunk + (k & 3) * 32, 16, 1024);
                     mma_bf16_ss(tmem + kTmemS + sb * kTileN, a, b, idesc_qk, k > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(B_S_FULL + sb));
@@ -414,18 +468,31 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         __syncwarp();
     } else {
         // ============================================================ softmax
-        const int h = tid;   // head row == TMEM lane
+        // Q rows of this head group (1 KB each), zero past the last head
+        {
+            const uint8_t* qb = reinterpret_cast<const uint8_t*>(p.q) + ((size_t)t * p.H + head0) * 1024;
+            for (int k = tid; k < kHG * 64; k += kSoftmaxWarps * 32) {
+                const int r = k >> 6, piece = k & 63;
+                const uint32_t dst = sQ + (piece >> 3) * kChunk + sw128(r, piece & 7);
+                const bool on = r < hcount && ntiles > 0;
+                cp_async_16(dst, on ? qb + (size_t)r * 1024 + piece * 16 : qb, on ? 16u : 0u);
+            }
+            cp_async_arrive_noinc(bar(B_Q_FULL));
+        }
+        // head row h lives in TMEM lane 32*warp + (h % 16) for M = 64; lanes
+        // 16..31 of each warp hold no row but join every warp-wide TMEM access
+        const bool owner = lane < 16;
+        const int h = warp * 16 + (lane & 15);
+        const bool live = owner && h < hcount;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const uint32_t peer_x = mapa(sX, peer);
-        const uint32_t peer_x_full = mapa(bar(B_X_FULL), peer);
-        const uint32_t peer_x_free = mapa(bar(B_X_FREE), peer);
-        const bool live = h < p.H;
         float m_run = -INFINITY, l_run = 0.f;
         for (int i = 0; i < ntiles; ++i) {
             const int sb = i & 1;
-            const int stage = i % kStages;
+            const int stage = i & 1;
             float s[64];
             wait_bar(bar(B_S_FULL + sb), (i >> 1) & 1, abort_flag);
+            if (tid == 0 && i < 8) DSV4_TR(28 + i);
+            __syncwarp();
             tc_fence_after();
             {
                 float a[32], b[32];
@@ -436,26 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             }
             tc_fence_before();
             mbar_arrive(bar(B_S_FREE + sb));
-            // exchange partial scores with the partner CTA (other row half)
-            if (i >= 1) wait_bar_cluster(bar(B_X_FREE), (i - 1) & 1, abort_flag);
-            if (live) {
-#pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    st_cluster_v4(peer_x + h * 256 + ((q ^ (h & 15)) << 4), s[4 * q], s[4 * q + 1],
-                                  s[4 * q + 2], s[4 * q + 3]);
-            }
-            mbar_arrive_cluster(peer_x_full);
-            wait_bar_cluster(bar(B_X_FULL), i & 1, abort_flag);
-            if (live) {
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float4 x = ld_shared_v4(sX + h * 256 + ((q ^ (h & 15)) << 4));
-                    s[4 * q] += x.x; s[4 * q + 1] += x.y; s[4 * q + 2] += x.z; s[4 * q + 3] += x.w;
-                }
-            }
-            mbar_arrive_cluster(peer_x_free);
-            // mask, scale to log2 units, online max with lazy rescaling
-            wait_bar(bar(B_MASK_FULL + stage), (i / kStages) & 1, abort_flag);
+            wait_bar(bar(B_MASK_FULL + stage), (i >> 1) & 1, abort_flag);
             const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + OFF_MASK + stage * 8);
             float mt = -INFINITY;
 #pragma unroll
@@ -463,137 +511,223 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 s[j] = ((mask >> j) & 1ull) ? s[j] * p.scale_log2 : -INFINITY;
                 mt = fmaxf(mt, s[j]);
             }
-            const float m_new = fmaxf(m_run, mt);
-            const bool rescale = m_new > m_run + kRescaleLog2;
+            const bool need = live && mt > m_run + kRescaleLog2;
             float alpha = 1.f;
-            if (rescale) {
-                alpha = fast_exp2(m_run - m_new);
-                m_run = m_new;
+            if (need) {
+                alpha = fast_exp2(m_run - mt);
+                m_run = mt;
             }
             uint32_t pk[32];
             float lsum = 0.f;
-            const bool any = m_run != -INFINITY;
+            const bool any = live && m_run != -INFINITY;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const float p0 = any ? fast_exp2(s[2 * j] - m_run) : 0.f;
                 const float p1 = any ? fast_exp2(s[2 * j + 1] - m_run) : 0.f;
-                __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
-                lsum += __low2float(v) + __high2float(v);
-                pk[j] = *reinterpret_cast<uint32_t*>(&v);
+                // the denominator sums the fp32 probabilities; the bf16 copies
+                // only feed the PV product
+                lsum += p0 + p1;
+                pk[j] = pack_bf16x2(p0, p1);
             }
             l_run = l_run * alpha + lsum;
-            if (rescale && i > 0) {
-                wait_bar(bar(B_P_FREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag);
-                tc_fence_after();
+            if (i > 0) {
+                // a head whose running max moved scales its O^T column; each
+                // softmax thread holds one value dim of O^T for all heads
+                if (bar_red_or(2, kSoftmaxWarps * 32, need)) {
+                    if (owner) wsm[h] = alpha;
+                    named_barrier_sync(2, kSoftmaxWarps * 32);
+                    wait_bar(bar(B_P_FREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag);
+                    __syncwarp();
+                    tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < 8; ++c) {
-                    float o[32];
-                    tmem_ld32(lane_addr + kTmemO + c * 32, o);
+                    for (int c = 0; c < 8; ++c) {
+                        float o[32];
+                        tmem_ld32(lane_addr + kTmemO + c * 32, o);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) o[j] *= alpha;
-                    tmem_st32(lane_addr + kTmemO + c * 32, o);
+                        for (int j = 0; j < 32; ++j) o[j] *= wsm[(c & 1) * 32 + j];
+                        tmem_st32(lane_addr + kTmemO + c * 32, o);
+                    }
                 }
             }
             if (i >= 2) wait_bar(bar(B_P_FREE + sb), ((i - 2) >> 1) & 1, abort_flag);
-            const uint32_t prow = sP + sb * kPBytes;
+            if (owner) {
+                const uint32_t prow = sP + sb * kPBytes;
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                st_shared_v4(prow + sw128(h, q), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                for (int q = 0; q < 8; ++q)
+                    st_shared_v4(prow + sw128(h, q), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
             fence_proxy_async();
             tc_fence_before();
             mbar_arrive(bar(B_P_FULL + sb));
+            if (tid == 0 && i < 8) DSV4_TR(44 + i);
         }
         if (ntiles > 0) {
             wait_bar(bar(B_O_FINAL), 0, abort_flag);
+            if (tid == 0) DSV4_TR(52);
             tc_fence_after();
             fence_proxy_async();
         }
-        ml[h] = make_float2(ntiles > 0 ? m_run : -INFINITY, ntiles > 0 ? l_run : 0.f);
+        if (owner) ml[h] = make_float2(live && ntiles > 0 ? m_run : -INFINITY, live && ntiles > 0 ? l_run : 0.f);
     }
 
     // ------------------------------------------------------------ merge
-    cluster_sync();   // A: every split of the cluster finished its key loop
+    cluster_sync();   // A: every slice of the cluster finished its key loop
+    if (tid == 0) DSV4_TR(53);
     const bool final_out = p.gsplits == 1;
+    // Slice cs owns the 8-dim units [u_lo, u_hi) of the output.  Each softmax
+    // thread holds one value dim of the weighted accumulator for all heads:
+    // dims this slice owns go into the local fp32 buffer T[dim][head]; the
+    // others go (bf16) to the workspace, where their owners read them after
+    // the cluster barrier (L2 moves these far faster than distributed shared
+    // memory does).
+    const int u_lo = (cs * 64) / Sc;
+    const int u_hi = ((cs + 1) * 64) / Sc;
+    float* T = reinterpret_cast<float*>(smem + OFF_MERGE);
+    uint16_t* mrg_t = p.merge + (((size_t)t * p.gsplits + gsplit) * G + grp) * Sc * (kDim * kHG);   // [slice][dim][head]
     if (warp < kSoftmaxWarps) {
-        const int h = tid;
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        if (h < p.H) {
+        const bool owner = lane < 16;
+        const int h = warp * 16 + (lane & 15);
+        const bool live = owner && h < hcount;
+        if (owner) {
+            // (m, l) of every slice of this head group, loads issued together
+            float2 mls[kMaxCluster];
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxCluster; ++s2)
+                mls[s2] = s2 < Sc ? *cluster_ptr(&ml[h], s2 * G + grp) : make_float2(-INFINITY, 0.f);
             float M = -INFINITY;
-            float2 mls[kMaxClusterSplits];
-            for (int s = 0; s < p.csplits; ++s) {
-                mls[s] = ld_cluster_v2(mapa(base + OFF_RING + h * 8, 2 * s + half));
-                M = fmaxf(M, mls[s].x);
-            }
-            const float sk = __ldg(p.sink + h) * kLog2e;
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxCluster; ++s2) M = fmaxf(M, mls[s2].x);
+            const float sk = live ? __ldg(p.sink + head0 + h) * kLog2e : -INFINITY;
             if (final_out) M = fmaxf(M, sk);
             float Lsum = 0.f;
             if (M != -INFINITY) {
-                for (int s = 0; s < p.csplits; ++s)
-                    if (mls[s].x != -INFINITY) Lsum += mls[s].y * exp2f(mls[s].x - M);
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxCluster; ++s2)
+                    if (mls[s2].x != -INFINITY) Lsum += mls[s2].y * exp2f(mls[s2].x - M);
                 if (final_out && sk != -INFINITY) Lsum += exp2f(sk - M);
             }
-            const float mine = mls[csplit].x;
-            const float alpha = (ntiles > 0 && Lsum > 0.f && mine != -INFINITY) ? exp2f(mine - M) / Lsum : 0.f;
-            for (int c = 0; c < 8; ++c) {
-                float o[32];
-                if (ntiles > 0) {
-                    tmem_ld32(lane_addr + kTmemO + c * 32, o);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) o[j] = 0.f;
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_shared_v4(sMerge + h * 1024 + (((c * 8 + q) ^ (h & 7)) << 4),
-                                 __float_as_uint(o[4 * q] * alpha), __float_as_uint(o[4 * q + 1] * alpha),
-                                 __float_as_uint(o[4 * q + 2] * alpha), __float_as_uint(o[4 * q + 3] * alpha));
-            }
-            if (rank == 0) {
+            const float mine = ml[h].x;
+            wsm[h] = (live && ntiles > 0 && Lsum > 0.f && mine != -INFINITY) ? exp2f(mine - M) / Lsum : 0.f;
+            if (live && cs == 0) {
                 if (final_out) {
-                    if (p.lse) p.lse[(size_t)t * p.H + h] = (Lsum > 0.f ? M + log2f(Lsum) : -INFINITY) * kLn2;
+                    if (p.lse)
+                        p.lse[(size_t)t * p.H + head0 + h] = (Lsum > 0.f ? M + log2f(Lsum) : -INFINITY) * kLn2;
                 } else {
-                    p.part_ml[((size_t)t * p.gsplits + gsplit) * p.H + h] = make_float2(M, Lsum);
+                    p.part_ml[((size_t)t * p.gsplits + gsplit) * p.H + head0 + h] = make_float2(M, Lsum);
                 }
             }
         }
-    }
-    tc_fence_before();
-    cluster_sync();   // B: every CTA's scaled accumulator is in its merge buffer
-    tc_fence_after();
-    {
-        // CTA (csplit, half) writes 8-column units [u0, u1) of its half.
-        const int u0 = (static_cast<int>(csplit) * 32) / p.csplits;
-        const int u1 = ((static_cast<int>(csplit) + 1) * 32) / p.csplits;
-        const int nu = u1 - u0;
-        const int items = p.H * nu;
-        for (int it = tid; it < items; it += kThreads) {
-            const int h = it / nu;
-            const int u = u0 + it % nu;
-            float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            for (int s = 0; s < p.csplits; ++s) {
-                const uint32_t rb = mapa(sMerge + h * 1024, 2 * s + half);
-                const float4 a = ld_cluster_v4(rb + (((2 * u) ^ (h & 7)) << 4));
-                const float4 b = ld_cluster_v4(rb + (((2 * u + 1) ^ (h & 7)) << 4));
-                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        named_barrier_sync(2, kSoftmaxWarps * 32);
+        if (tid == 0) DSV4_TR(59);
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        __syncwarp();
+#pragma unroll 1
+        for (int mt = 0; mt < 4; ++mt) {
+            float o[64];
+            if (ntiles > 0) {
+                float a[32], b[32];
+                tmem_ld32(lane_addr + kTmemO + mt * kHG, a);
+                tmem_ld32(lane_addr + kTmemO + mt * kHG + 32, b);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) { o[j] = a[j] * wsm[j]; o[32 + j] = b[j] * wsm[32 + j]; }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) o[j] = 0.f;
             }
-            const size_t col = (size_t)half * 256 + u * 8;
+            const int d = mt * 128 + warp * 32 + lane;           // this thread's value dim
+            const int u = d >> 3;
+            if (u >= u_lo && u < u_hi) {
+                const int dl = d - 8 * u_lo;
+                float* row = T + dl * kHG;
+#pragma unroll
+                for (int q = 0; q < 16; ++q)   // 16-byte chunk q of the row, swizzled by dim
+                    *reinterpret_cast<float4*>(row + 4 * (q ^ (dl & 15))) =
+                        make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            } else {
+                uint4* dst = reinterpret_cast<uint4*>(mrg_t + ((size_t)cs * kDim + d) * kHG);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    dst[q] = make_uint4(pack_bf16x2(o[8 * q], o[8 * q + 1]), pack_bf16x2(o[8 * q + 2], o[8 * q + 3]),
+                                        pack_bf16x2(o[8 * q + 4], o[8 * q + 5]),
+                                        pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
+            }
+        }
+    }
+    if (tid == 0) DSV4_TR(60);
+    tc_fence_before();
+    cluster_sync();   // B: every slice's contribution is in the workspace / local buffer
+    tc_fence_after();
+    if (tid == 0) DSV4_TR(55);
+    const int nd = 8 * (u_hi - u_lo);                             // dims this slice owns
+    if (Sc > 1) {
+        // add the other slices' bf16 contributions: chunk k = (dim, 8 heads)
+        for (int k = tid; k < nd * 8; k += kThreads) {
+            const int dl = k >> 3, c8 = k & 7;
+            float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            for (int s2 = 0; s2 < Sc; ++s2) {
+                if (s2 == cs) continue;
+                const uint4 v = *reinterpret_cast<const uint4*>(
+                    mrg_t + ((size_t)s2 * kDim + 8 * u_lo + dl) * kHG + 8 * c8);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[2 * e] += __uint_as_float(w[e] << 16);
+                    acc[2 * e + 1] += __uint_as_float(w[e] & 0xffff0000u);
+                }
+            }
+            float* row = T + dl * kHG;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float4* cell = reinterpret_cast<float4*>(row + 4 * ((2 * c8 + hf) ^ (dl & 15)));
+                float4 x = *cell;
+                x.x += acc[4 * hf]; x.y += acc[4 * hf + 1]; x.z += acc[4 * hf + 2]; x.w += acc[4 * hf + 3];
+                *cell = x;
+            }
+        }
+        __syncthreads();
+        // the partials are dead: drop their L2 lines without writing them back
+        for (int ln = tid; ln < (Sc - 1) * nd; ln += kThreads) {
+            int s2 = ln / nd;
+            if (s2 >= cs) ++s2;
+            const int dl = ln % nd;
+            const uint16_t* lp = mrg_t + ((size_t)s2 * kDim + 8 * u_lo + dl) * kHG;   // one 128-byte line
+            asm volatile("discard.global.L2 [%0], 128;" ::"l"(lp) : "memory");
+        }
+    } else {
+        __syncthreads();
+    }
+    {
+        // output: item (head, 8 dims) from T (consecutive threads: consecutive heads)
+        const int items = hcount * (u_hi - u_lo);
+        for (int it = tid; it < items; it += kThreads) {
+            const int hh = it % hcount;
+            const int u = u_lo + it / hcount;
+            const int dl0 = 8 * (u - u_lo);
+            float acc[8];
+#pragma unroll
+            for (int k2 = 0; k2 < 8; ++k2) {
+                const int dl = dl0 + k2;
+                acc[k2] = T[dl * kHG + 4 * ((hh >> 2) ^ (dl & 15)) + (hh & 3)];
+            }
+            const size_t rowoff = ((size_t)t * p.H + head0 + hh) * kDim + u * 8;
             if (final_out) {
                 uint4 v;
                 v.x = pack_bf16x2(acc[0], acc[1]);
                 v.y = pack_bf16x2(acc[2], acc[3]);
                 v.z = pack_bf16x2(acc[4], acc[5]);
                 v.w = pack_bf16x2(acc[6], acc[7]);
-                *reinterpret_cast<uint4*>(p.out + ((size_t)t * p.H + h) * kDim + col) = v;
+                *reinterpret_cast<uint4*>(p.out + rowoff) = v;
             } else {
-                float* dst = p.part_o + (((size_t)t * p.gsplits + gsplit) * p.H + h) * kDim + col;
+                float* dst = p.part_o + (((size_t)t * p.gsplits + gsplit) * p.H + head0 + hh) * kDim + u * 8;
                 *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
                 *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
             }
         }
     }
     if (err) atomicOr(&g_dev_error, err);
+    if (tid == 0) DSV4_TR(56);
     cluster_sync();   // C: peers are done reading this CTA's shared memory
+    if (tid == 0) DSV4_TR(57);
     if (warp == kMmaWarp) {
         if (*reinterpret_cast<volatile int*>(abort_flag)) {
             // a wait gave up: give in-flight tensor-core work time to drain
@@ -646,7 +780,7 @@ __global__ void __launch_bounds__(256) dsv4_combine_kernel(const __grid_constant
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;
-    int max_clusters[kMaxClusterSplits + 1] = {0, 0, 0, 0, 0};
+    int max_clusters[kMaxCluster + 1] = {0, 0, 0, 0, 0, 0, 0, 0, 0};   // by cluster size
 };
 constexpr int kMaxDevices = 64;
 static DeviceInfo g_devinfo[kMaxDevices];
@@ -662,14 +796,14 @@ static int device_info(DeviceInfo& out) {
         auto kern = dsv4_attn_kernel<DSV4_KV_BF16>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) != cudaSuccess)
             return DSV4_ERR_CUDA;
-        for (int sc = 1; sc <= kMaxClusterSplits; ++sc) {
+        for (int cl = 1; cl <= kMaxCluster; ++cl) {
             cudaLaunchConfig_t cfg = {};
             cudaLaunchAttribute attr[1];
-            cfg.gridDim = dim3(2 * sc, 1, 1);
+            cfg.gridDim = dim3(cl, 1, 1);
             cfg.blockDim = dim3(kThreads, 1, 1);
             cfg.dynamicSmemBytes = kSmemAlloc;
             attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2 * sc;
+            attr[0].val.clusterDim.x = cl;
             attr[0].val.clusterDim.y = 1;
             attr[0].val.clusterDim.z = 1;
             cfg.attrs = attr;
@@ -677,9 +811,9 @@ static int device_info(DeviceInfo& out) {
             int n = 0;
             if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
                 cudaGetLastError();
-                n = di.sms / (2 * sc) * 3 / 4;
+                n = di.sms / cl * 3 / 4;
             }
-            di.max_clusters[sc] = n > 0 ? n : 1;
+            di.max_clusters[cl] = n > 0 ? n : 1;
         }
         di.ready = true;
     }
@@ -692,13 +826,15 @@ static int list_max(int ratio, int window, int topk, int max_seq_len) {
     return window + extra;
 }
 
-// Split plan: cluster splits sc (merged on chip) x grid splits sg (merged by
-// the combine kernel), chosen to minimise waves x tiles per split.
-static int make_plan(int T, int lmax, int num_splits, const DeviceInfo& di, int& sc, int& sg) {
+// Split plan: Sc key slices merged inside the kernel (one cluster of Sc x G
+// CTAs, G head groups) times Sg cluster groups merged by the combine kernel,
+// chosen to minimise waves x tiles per slice.
+static int make_plan(int T, int G, int lmax, int num_splits, const DeviceInfo& di, int& sc, int& sg) {
     const int tiles_total = (lmax + kTileN - 1) / kTileN;
+    const int max_sc = kMaxCluster / G;
     if (num_splits > 0) {
         sc = 1;
-        for (int c = kMaxClusterSplits; c >= 1; --c)
+        for (int c = max_sc; c >= 1; --c)
             if (num_splits % c == 0) { sc = c; break; }
         sg = num_splits / sc;
         return DSV4_OK;
@@ -706,15 +842,16 @@ static int make_plan(int T, int lmax, int num_splits, const DeviceInfo& di, int&
     double best = 1e30;
     sc = 1;
     sg = 1;
-    for (int c = 1; c <= kMaxClusterSplits; ++c) {
+    for (int c = 1; c <= max_sc; ++c) {
+        const int per_wave = di.max_clusters[c * G];
         for (int g = 1; g <= 64; ++g) {
             const int s = c * g;
             if (s > 1 && s > tiles_total) break;
             const long long clusters = (long long)T * g;
-            if (g > 1 && clusters > 4LL * di.max_clusters[c]) break;
-            const long long waves = (clusters + di.max_clusters[c] - 1) / di.max_clusters[c];
-            const int tiles = (tiles_total + s - 1) / s;
-            const double cost = (double)waves * (tiles + 1) + (g > 1 ? 3.0 : 0.0) + 0.25 * (c - 1);
+            if (g > 1 && clusters > 4LL * per_wave) break;
+            const long long waves = (clusters + per_wave - 1) / per_wave;
+            const double tiles = (double)lmax / s / kTileN;
+            const double cost = (double)waves * (tiles + 1.5) + (g > 1 ? 3.0 : 0.0) + 0.5 * (c - 1);
             if (cost < best - 1e-9) { best = cost; sc = c; sg = g; }
         }
     }
@@ -735,9 +872,20 @@ static int check_pool(const dsv4_kv_pool* pool) {
     return DSV4_OK;
 }
 
-static size_t workspace_bytes_for(int T, int H, int sg) {
+// Workspace: [fp32 partial outputs and (m, l) of each cluster group when
+// Sg > 1][bf16 per-slice accumulators exchanged inside a cluster when Sc > 1].
+static size_t ws_part_bytes(int T, int H, int sg) {
     if (sg <= 1) return 0;
-    return (size_t)T * sg * H * kDim * sizeof(float) + (size_t)T * sg * H * sizeof(float2) + 256;
+    return ((size_t)T * sg * H * kDim * sizeof(float) + (size_t)T * sg * H * sizeof(float2) + 255) & ~size_t(255);
+}
+static size_t ws_merge_bytes(int T, int G, int sc, int sg) {
+    if (sc <= 1) return 0;
+    return (size_t)T * sg * G * sc * kDim * kHG * sizeof(uint16_t);
+}
+static size_t workspace_bytes_for(int T, int H, int sc, int sg) {
+    const int G = (H + kHG - 1) / kHG;
+    const size_t n = ws_part_bytes(T, H, sg) + ws_merge_bytes(T, G, sc, sg);
+    return n ? n + 256 : 0;
 }
 
 struct Call {
@@ -764,7 +912,7 @@ struct Call {
 
 static int run(const Call& c) {
     if (!c.q || !c.out || !c.seq_lens || !c.sink) return DSV4_ERR_INVALID;
-    if (c.T < 1 || c.batch < 1 || c.H < 1 || c.H > kM || c.window < 1) return DSV4_ERR_INVALID;
+    if (c.T < 1 || c.batch < 1 || c.H < 1 || c.H > 2 * kHG || c.window < 1) return DSV4_ERR_INVALID;
     if (!std::isfinite(c.scale)) return DSV4_ERR_INVALID;
     if (c.T > 65535) return DSV4_ERR_UNSUPPORTED;
     if (c.ratio != 0 && c.ratio != 4 && c.ratio != 128) return DSV4_ERR_UNSUPPORTED;
@@ -784,12 +932,13 @@ static int run(const Call& c) {
     rc = device_info(di);
     if (rc) return rc;
     const int lmax = list_max(c.ratio, c.window, c.topk, c.max_seq_len);
+    const int G = (c.H + kHG - 1) / kHG;
     int sc = 1, sg = 1;
-    make_plan(c.T, lmax, c.num_splits, di, sc, sg);
+    make_plan(c.T, G, lmax, c.num_splits, di, sc, sg);
     const int splits = sc * sg;
-    const int chunk = ((lmax + splits - 1) / splits + kTileN - 1) / kTileN * kTileN;
+    const int chunk = (lmax + splits - 1) / splits;   // key slots per slice
     if (c.T * (long long)sg > 65535) return DSV4_ERR_UNSUPPORTED;
-    const size_t need = workspace_bytes_for(c.T, c.H, sg);
+    const size_t need = workspace_bytes_for(c.T, c.H, sc, sg);
     if (need > 0 && (!c.ws || c.ws_bytes < need)) return DSV4_ERR_WORKSPACE;
 
     Params p;
@@ -798,6 +947,7 @@ static int run(const Call& c) {
     p.T = c.T;
     p.H = c.H;
     p.batch = c.batch;
+    p.groups = G;
     p.seq_lens = c.seq_lens;
     p.cu_seqlens = c.cu;
     p.rpi = c.rpi;
@@ -826,10 +976,13 @@ static int run(const Call& c) {
     p.gsplits = sg;
     p.out = static_cast<__nv_bfloat16*>(c.out);
     p.lse = c.lse;
-    if (sg > 1) {
-        uintptr_t w = (reinterpret_cast<uintptr_t>(c.ws) + 255) & ~uintptr_t(255);
-        p.part_o = reinterpret_cast<float*>(w);
-        p.part_ml = reinterpret_cast<float2*>(w + (size_t)c.T * sg * c.H * kDim * sizeof(float));
+    if (need > 0) {
+        const uintptr_t w = (reinterpret_cast<uintptr_t>(c.ws) + 255) & ~uintptr_t(255);
+        if (sg > 1) {
+            p.part_o = reinterpret_cast<float*>(w);
+            p.part_ml = reinterpret_cast<float2*>(w + (size_t)c.T * sg * c.H * kDim * sizeof(float));
+        }
+        if (sc > 1) p.merge = reinterpret_cast<uint16_t*>(w + ws_part_bytes(c.T, c.H, sg));
     }
     p.debug_rows = c.debug_rows;
     p.debug_stride = lmax;
@@ -837,12 +990,12 @@ static int run(const Call& c) {
     cudaStream_t st = static_cast<cudaStream_t>(c.stream);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3(2 * sc, c.T, sg);
+    cfg.gridDim = dim3(sc * G, c.T, sg);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemAlloc;
     cfg.stream = st;
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2 * sc;
+    attr[0].val.clusterDim.x = sc * G;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -911,7 +1064,7 @@ int dsv4_attn_verify(const void* q, int32_t num_tokens, int32_t batch, int32_t n
 int dsv4_attn_plan(int32_t num_tokens, int32_t num_heads, int32_t compress_ratio, int32_t window,
                    int32_t topk, int32_t max_seq_len, int32_t num_splits, int32_t* cluster_splits,
                    int32_t* grid_splits) {
-    if (num_tokens < 1 || num_heads < 1 || num_heads > dsv4::kM || window < 1 || num_splits < 0 ||
+    if (num_tokens < 1 || num_heads < 1 || num_heads > 2 * dsv4::kHG || window < 1 || num_splits < 0 ||
         !cluster_splits || !grid_splits)
         return DSV4_ERR_INVALID;
     if (compress_ratio != 0 && compress_ratio != 4 && compress_ratio != 128) return DSV4_ERR_UNSUPPORTED;
@@ -919,7 +1072,8 @@ int dsv4_attn_plan(int32_t num_tokens, int32_t num_heads, int32_t compress_ratio
     int rc = dsv4::device_info(di);
     if (rc) return rc;
     int sc = 1, sg = 1;
-    dsv4::make_plan(num_tokens, dsv4::list_max(compress_ratio, window, topk, max_seq_len), num_splits, di, sc, sg);
+    dsv4::make_plan(num_tokens, (num_heads + dsv4::kHG - 1) / dsv4::kHG,
+                    dsv4::list_max(compress_ratio, window, topk, max_seq_len), num_splits, di, sc, sg);
     *cluster_splits = sc;
     *grid_splits = sg;
     return DSV4_OK;
@@ -930,7 +1084,7 @@ size_t dsv4_attn_workspace_size(int32_t num_tokens, int32_t num_heads, int32_t c
     int32_t sc = 1, sg = 1;
     if (dsv4_attn_plan(num_tokens, num_heads, compress_ratio, window, topk, max_seq_len, num_splits, &sc, &sg))
         return 0;
-    return dsv4::workspace_bytes_for(num_tokens, num_heads, sg);
+    return dsv4::workspace_bytes_for(num_tokens, num_heads, sc, sg);
 }
 
 int dsv4_attn_get_device_error(uint32_t* flags, void* stream) {
@@ -944,6 +1098,15 @@ int dsv4_attn_get_device_error(uint32_t* flags, void* stream) {
     *flags = v;
     return DSV4_OK;
 }
+
+#ifdef DSV4_TRACE
+int dsv4_attn_trace_read(void* host, size_t bytes) {
+    if (bytes > sizeof(dsv4::g_trace)) bytes = sizeof(dsv4::g_trace);
+    if (cudaDeviceSynchronize() != cudaSuccess) return DSV4_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(host, dsv4::g_trace, bytes) != cudaSuccess) return DSV4_ERR_CUDA;
+    return DSV4_OK;
+}
+#endif
 
 const char* dsv4_attn_strerror(int status) {
     switch (status) {

@@ -89,6 +89,7 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
     return r;
 }
 __device__ __forceinline__ void cluster_sync() {
+    __syncwarp();
     asm volatile("barrier.cluster.arrive.release.aligned;\n"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
