@@ -84,15 +84,19 @@ enum Bar {
     B_P_FULL = B_S_FREE + 2,
     B_P_FREE = B_P_FULL + 2,
     B_O_FINAL = B_P_FREE + 2,
+    B_MERGE,                                   // peers' partials staged by bulk copy
     B_COUNT
 };
 constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;
 constexpr int OFF_MERGE = OFF_KV;              // [owned dim][64 heads] fp32, reuses the KV stages
+                                               // (peers' bf16 blocks are staged in the Q area)
 constexpr int kSmemUsed = OFF_MISC + 16;
 constexpr int kSmemAlloc = kSmemUsed + 1024;   // room to align the base to 1024 bytes
 static_assert(OFF_MERGE + kDim * kHG * 4 <= OFF_P, "merge buffer must fit in the KV stages");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 static_assert(kRing % kLoadThreads == 0, "ring slots per loader thread");
+static_assert(6 * 80 * 128 <= kQBytes, "staged peer blocks (at most 6 x 80 dims, Sc = 7) must fit in the Q area");
+static_assert(kMaxCluster * kHG * 4 <= kRing * 4, "merge weights must fit in the ring");
 
 __device__ unsigned int g_dev_error;
 
@@ -326,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             mbar_init(bar(B_P_FREE + s), 1);
         }
         mbar_init(bar(B_O_FINAL), 1);
+        mbar_init(bar(B_MERGE), 1);
         fence_mbar_init_cluster();
         *abort_flag = 0;
     }
@@ -568,58 +573,15 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             fence_proxy_async();
         }
         if (owner) ml[h] = make_float2(live && ntiles > 0 ? m_run : -INFINITY, live && ntiles > 0 ? l_run : 0.f);
-    }
-
-    // ------------------------------------------------------------ merge
-    cluster_sync();   // A: every slice of the cluster finished its key loop
-    if (tid == 0) DSV4_TR(53);
-    const bool final_out = p.gsplits == 1;
-    // Slice cs owns the 8-dim units [u_lo, u_hi) of the output.  Each softmax
-    // thread holds one value dim of the weighted accumulator for all heads:
-    // dims this slice owns go into the local fp32 buffer T[dim][head]; the
-    // others go (bf16) to the workspace, where their owners read them after
-    // the cluster barrier (L2 moves these far faster than distributed shared
-    // memory does).
-    const int u_lo = (cs * 64) / Sc;
-    const int u_hi = ((cs + 1) * 64) / Sc;
-    float* T = reinterpret_cast<float*>(smem + OFF_MERGE);
-    uint16_t* mrg_t = p.merge + (((size_t)t * p.gsplits + gsplit) * G + grp) * Sc * (kDim * kHG);   // [slice][dim][head]
-    if (warp < kSoftmaxWarps) {
-        const bool owner = lane < 16;
-        const int h = warp * 16 + (lane & 15);
-        const bool live = owner && h < hcount;
-        if (owner) {
-            // (m, l) of every slice of this head group, loads issued together
-            float2 mls[kMaxCluster];
-#pragma unroll
-            for (int s2 = 0; s2 < kMaxCluster; ++s2)
-                mls[s2] = s2 < Sc ? *cluster_ptr(&ml[h], s2 * G + grp) : make_float2(-INFINITY, 0.f);
-            float M = -INFINITY;
-#pragma unroll
-            for (int s2 = 0; s2 < kMaxCluster; ++s2) M = fmaxf(M, mls[s2].x);
-            const float sk = live ? __ldg(p.sink + head0 + h) * kLog2e : -INFINITY;
-            if (final_out) M = fmaxf(M, sk);
-            float Lsum = 0.f;
-            if (M != -INFINITY) {
-#pragma unroll
-                for (int s2 = 0; s2 < kMaxCluster; ++s2)
-                    if (mls[s2].x != -INFINITY) Lsum += mls[s2].y * exp2f(mls[s2].x - M);
-                if (final_out && sk != -INFINITY) Lsum += exp2f(sk - M);
-            }
-            const float mine = ml[h].x;
-            wsm[h] = (live && ntiles > 0 && Lsum > 0.f && mine != -INFINITY) ? exp2f(mine - M) / Lsum : 0.f;
-            if (live && cs == 0) {
-                if (final_out) {
-                    if (p.lse)
-                        p.lse[(size_t)t * p.H + head0 + h] = (Lsum > 0.f ? M + log2f(Lsum) : -INFINITY) * kLn2;
-                } else {
-                    p.part_ml[((size_t)t * p.gsplits + gsplit) * p.H + head0 + h] = make_float2(M, Lsum);
-                }
-            }
-        }
-        named_barrier_sync(2, kSoftmaxWarps * 32);
-        if (tid == 0) DSV4_TR(59);
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        // Slice cs owns the 8-dim units [u_lo, u_hi) of the output.  Each
+        // softmax thread holds one value dim of this slice's (unnormalised)
+        // accumulator for all heads: owned dims go to the local fp32 buffer
+        // T[dim][head]; the others go (bf16) to the workspace, where their
+        // owners fetch them after the cluster barrier (L2 and bulk copies move
+        // these far faster than distributed shared memory does).
+        const int u_lo = (cs * 64) / Sc, u_hi = ((cs + 1) * 64) / Sc;
+        float* T = reinterpret_cast<float*>(smem + OFF_MERGE);
+        uint16_t* mrg_t = p.merge + (((size_t)t * p.gsplits + gsplit) * G + grp) * Sc * (kDim * kHG);
         __syncwarp();
 #pragma unroll 1
         for (int mt = 0; mt < 4; ++mt) {
@@ -629,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 tmem_ld32(lane_addr + kTmemO + mt * kHG, a);
                 tmem_ld32(lane_addr + kTmemO + mt * kHG + 32, b);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) { o[j] = a[j] * wsm[j]; o[32 + j] = b[j] * wsm[32 + j]; }
+                for (int j = 0; j < 32; ++j) { o[j] = a[j]; o[32 + j] = b[j]; }
             } else {
 #pragma unroll
                 for (int j = 0; j < 64; ++j) o[j] = 0.f;
@@ -653,61 +615,105 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             }
         }
     }
+
+    // ------------------------------------------------------------ merge
     if (tid == 0) DSV4_TR(60);
     tc_fence_before();
-    cluster_sync();   // B: every slice's contribution is in the workspace / local buffer
+    cluster_sync();   // B: every slice's accumulator and (m, l) are published
     tc_fence_after();
     if (tid == 0) DSV4_TR(55);
-    const int nd = 8 * (u_hi - u_lo);                             // dims this slice owns
-    if (Sc > 1) {
-        // add the other slices' bf16 contributions: chunk k = (dim, 8 heads)
-        for (int k = tid; k < nd * 8; k += kThreads) {
-            const int dl = k >> 3, c8 = k & 7;
-            float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            for (int s2 = 0; s2 < Sc; ++s2) {
-                if (s2 == cs) continue;
-                const uint4 v = *reinterpret_cast<const uint4*>(
-                    mrg_t + ((size_t)s2 * kDim + 8 * u_lo + dl) * kHG + 8 * c8);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const bool final_out = p.gsplits == 1;
+    const int u_lo = (cs * 64) / Sc, u_hi = ((cs + 1) * 64) / Sc;
+    const int nd = 8 * (u_hi - u_lo);                                // dims this slice owns
+    const int dmax = 8 * ((64 + Sc - 1) / Sc);
+    const float* T = reinterpret_cast<const float*>(smem + OFF_MERGE);
+    const uint8_t* stage_in = smem + OFF_Q;                          // peers' bf16 blocks [slot][dim][head]
+    float* W = reinterpret_cast<float*>(smem + OFF_RING);            // [slice][head] merge weights
+    const uint16_t* mrg_t = p.merge + (((size_t)t * p.gsplits + gsplit) * G + grp) * Sc * (kDim * kHG);
+    if (Sc > 1 && tid == kMmaWarp * 32) {
+        // fetch this slice's dims from every other slice: one contiguous block each
+        const uint32_t mb = bar(B_MERGE);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb),
+                     "r"(static_cast<uint32_t>((Sc - 1) * nd * 128))
+                     : "memory");
+        int slot = 0;
+        for (int s2 = 0; s2 < Sc; ++s2) {
+            if (s2 == cs) continue;
+            const uint16_t* src = mrg_t + ((size_t)s2 * kDim + 8 * u_lo) * kHG;
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                             sQ + slot * dmax * 128),
+                         "l"(src), "r"(static_cast<uint32_t>(nd * 128)), "r"(mb)
+                         : "memory");
+            ++slot;
+        }
+    }
+    if (warp < kSoftmaxWarps && lane < 16) {
+        // weights of every slice's accumulator for head h: exp(m_s - M) / L
+        const int h = warp * 16 + lane;
+        const bool live = h < hcount;
+        float2 mls[kMaxCluster];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    acc[2 * e] += __uint_as_float(w[e] << 16);
-                    acc[2 * e + 1] += __uint_as_float(w[e] & 0xffff0000u);
-                }
-            }
-            float* row = T + dl * kHG;
+        for (int s2 = 0; s2 < kMaxCluster; ++s2)
+            mls[s2] = s2 < Sc ? *cluster_ptr(&ml[h], s2 * G + grp) : make_float2(-INFINITY, 0.f);
+        float M = -INFINITY;
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                float4* cell = reinterpret_cast<float4*>(row + 4 * ((2 * c8 + hf) ^ (dl & 15)));
-                float4 x = *cell;
-                x.x += acc[4 * hf]; x.y += acc[4 * hf + 1]; x.z += acc[4 * hf + 2]; x.w += acc[4 * hf + 3];
-                *cell = x;
+        for (int s2 = 0; s2 < kMaxCluster; ++s2) M = fmaxf(M, mls[s2].x);
+        const float sk = live ? __ldg(p.sink + head0 + h) * kLog2e : -INFINITY;
+        if (final_out) M = fmaxf(M, sk);
+        float Lsum = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxCluster; ++s2)
+                if (mls[s2].x != -INFINITY) Lsum += mls[s2].y * exp2f(mls[s2].x - M);
+            if (final_out && sk != -INFINITY) Lsum += exp2f(sk - M);
+        }
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxCluster; ++s2)
+            if (s2 < Sc)
+                W[s2 * kHG + h] = (live && Lsum > 0.f && mls[s2].x != -INFINITY) ? exp2f(mls[s2].x - M) / Lsum : 0.f;
+        if (live && cs == 0) {
+            if (final_out) {
+                if (p.lse) p.lse[(size_t)t * p.H + head0 + h] = (Lsum > 0.f ? M + log2f(Lsum) : -INFINITY) * kLn2;
+            } else {
+                p.part_ml[((size_t)t * p.gsplits + gsplit) * p.H + head0 + h] = make_float2(M, Lsum);
             }
         }
-        __syncthreads();
-        // the partials are dead: drop their L2 lines without writing them back
+    }
+    __syncthreads();
+    if (Sc > 1) {
+        wait_bar(bar(B_MERGE), 0, abort_flag);
+        // the workspace lines just copied are dead: drop them without write-back
         for (int ln = tid; ln < (Sc - 1) * nd; ln += kThreads) {
             int s2 = ln / nd;
             if (s2 >= cs) ++s2;
-            const int dl = ln % nd;
-            const uint16_t* lp = mrg_t + ((size_t)s2 * kDim + 8 * u_lo + dl) * kHG;   // one 128-byte line
+            const uint16_t* lp = mrg_t + ((size_t)s2 * kDim + 8 * u_lo + ln % nd) * kHG;   // one 128-byte line
             asm volatile("discard.global.L2 [%0], 128;" ::"l"(lp) : "memory");
         }
-    } else {
-        __syncthreads();
     }
+    if (tid == 0) DSV4_TR(59);
     {
-        // output: item (head, 8 dims) from T (consecutive threads: consecutive heads)
+        // output: item (head, 8 dims), consecutive threads on consecutive heads
         const int items = hcount * (u_hi - u_lo);
         for (int it = tid; it < items; it += kThreads) {
             const int hh = it % hcount;
             const int u = u_lo + it / hcount;
             const int dl0 = 8 * (u - u_lo);
+            const float wown = W[cs * kHG + hh];
             float acc[8];
 #pragma unroll
             for (int k2 = 0; k2 < 8; ++k2) {
                 const int dl = dl0 + k2;
-                acc[k2] = T[dl * kHG + 4 * ((hh >> 2) ^ (dl & 15)) + (hh & 3)];
+                acc[k2] = wown * T[dl * kHG + 4 * ((hh >> 2) ^ (dl & 15)) + (hh & 3)];
+            }
+            int slot = 0;
+            for (int s2 = 0; s2 < Sc; ++s2) {
+                if (s2 == cs) continue;
+                const float ws = W[s2 * kHG + hh];
+                const uint16_t* blk = reinterpret_cast<const uint16_t*>(stage_in + slot * dmax * 128);
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2)
+                    acc[k2] += ws * __uint_as_float(static_cast<uint32_t>(blk[(dl0 + k2) * kHG + hh]) << 16);
+                ++slot;
             }
             const size_t rowoff = ((size_t)t * p.H + head0 + hh) * kDim + u * 8;
             if (final_out) {
