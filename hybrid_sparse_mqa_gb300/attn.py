@@ -31,8 +31,9 @@ DEV_ERR = {
 EXPORTED = [
     "dsv4_attn_swa", "dsv4_attn_c4_sparse", "dsv4_attn_c128_dense", "dsv4_attn_verify",
     "dsv4_attn_plan", "dsv4_attn_workspace_size", "dsv4_attn_get_device_error",
-    "dsv4_attn_strerror",
+    "dsv4_attn_strerror", "dsv4_attn_c4_sparse_noalloc",
 ]
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class KvPool(ctypes.Structure):
@@ -63,7 +64,9 @@ def load_library(path=LIB_PATH):
     lib.dsv4_attn_c128_dense.argtypes = [P, I32, I32, P, P, PP, I32, PP, I32, P, F32, P, P, I32, P, SZ, P, P]
     lib.dsv4_attn_verify.argtypes = [P, I32, I32, I32, P, P, P, PP, I32, I32, PP, P, I32, I32, P, F32,
                                      P, P, I32, P, SZ, P, P]
-    for name in ("dsv4_attn_swa", "dsv4_attn_c4_sparse", "dsv4_attn_c128_dense", "dsv4_attn_verify"):
+    lib.dsv4_attn_c4_sparse_noalloc.argtypes = [P, I32, I32, P, P, PP, I32, PP, P, I32, P, F32, P, P, I32, P, P]
+    for name in ("dsv4_attn_swa", "dsv4_attn_c4_sparse", "dsv4_attn_c128_dense", "dsv4_attn_verify",
+                 "dsv4_attn_c4_sparse_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     lib.dsv4_attn_plan.argtypes = [I32, I32, I32, I32, I32, I32, I32,
                                    ctypes.POINTER(I32), ctypes.POINTER(I32)]
@@ -166,6 +169,23 @@ def dsv4_attn_c4_sparse(q, seq_lens, swa_pool, extra_pool, topk_idx, sink, *,
                                      ctypes.byref(swa_pool), window, ctypes.byref(extra_pool),
                                      _ptr(topk_idx), topk, _ptr(sink), scale, _ptr(out), _ptr(lse),
                                      num_splits, _ptr(workspace), wsb, _ptr(debug_rows), _stream(stream)))
+    return out, lse
+
+
+def dsv4_attn_c4_sparse_noalloc(q, seq_lens, swa_pool, extra_pool, topk_idx, sink, *,
+                                scale=1.0 / math.sqrt(512), window=128, req_pool_indices=None,
+                                out=None, lse=None, num_splits=0, debug_rows=None, stream=None):
+    """dsv4_attn_c4_sparse without a workspace argument: for callers that
+    cannot allocate device memory, the split merge uses the library's own
+    static scratch buffer (see include/dsv4attn.h for its limits)."""
+    T, H = q.shape[0], q.shape[1]
+    topk = topk_idx.shape[1]
+    if out is None or lse is None:
+        out, lse = _outputs(q, out, lse)
+    _check(lib().dsv4_attn_c4_sparse_noalloc(_ptr(q), T, H, _ptr(seq_lens), _ptr(req_pool_indices),
+                                             ctypes.byref(swa_pool), window, ctypes.byref(extra_pool),
+                                             _ptr(topk_idx), topk, _ptr(sink), scale, _ptr(out), _ptr(lse),
+                                             num_splits, _ptr(debug_rows), _stream(stream)))
     return out, lse
 
 

@@ -1017,6 +1017,29 @@ static int run(const Call& c) {
     return DSV4_OK;
 }
 
+// Scratch for dsv4_attn_c4_sparse_noalloc: a library-owned device buffer so
+// that callers without an allocator can still run split plans.  Host code sees
+// only a stand-in for this symbol; the device address is looked up per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DSV4_NOALLOC_SCRATCH_BYTES];
+static void* g_noalloc_addr[kMaxDevices];
+static std::mutex g_noalloc_mu;
+
+static int noalloc_scratch(void** addr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSV4_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return DSV4_ERR_CUDA;
+        }
+        g_noalloc_addr[dev] = ptr;
+    }
+    *addr = g_noalloc_addr[dev];
+    return DSV4_OK;
+}
+
 }  // namespace dsv4
 
 using dsv4::Call;
@@ -1105,6 +1128,26 @@ int dsv4_attn_get_device_error(uint32_t* flags, void* stream) {
     return DSV4_OK;
 }
 
+int dsv4_attn_c4_sparse_noalloc(const void* q, int32_t batch, int32_t num_heads, const int32_t* seq_lens,
+                                const int32_t* req_pool_indices, const dsv4_kv_pool* swa, int32_t window,
+                                const dsv4_kv_pool* extra, const int32_t* topk_idx, int32_t topk,
+                                const float* sink, float scale, void* out, float* lse, int32_t num_splits,
+                                int32_t* debug_rows, void* stream) {
+    if (batch < 1 || num_heads < 1 || num_heads > 2 * dsv4::kHG || window < 1 || topk < 1 || num_splits < 0)
+        return DSV4_ERR_INVALID;
+    const size_t need = dsv4_attn_workspace_size(batch, num_heads, 4, window, topk, 0, num_splits);
+    if (need > DSV4_NOALLOC_SCRATCH_BYTES) return DSV4_ERR_SCRATCH_LIMIT;
+    void* scratch = nullptr;
+    if (need > 0) {
+        const int rc = dsv4::noalloc_scratch(&scratch);
+        if (rc) return rc;
+    }
+    Call c{q, batch, batch, num_heads, seq_lens, nullptr, req_pool_indices, swa, window, 4, extra,
+           topk_idx, topk, 0, sink, scale, out, lse, num_splits, scratch,
+           need > 0 ? static_cast<size_t>(DSV4_NOALLOC_SCRATCH_BYTES) : 0, debug_rows, stream};
+    return dsv4::run(c);
+}
+
 #ifdef DSV4_TRACE
 int dsv4_attn_trace_read(void* host, size_t bytes) {
     if (bytes > sizeof(dsv4::g_trace)) bytes = sizeof(dsv4::g_trace);
@@ -1121,6 +1164,7 @@ const char* dsv4_attn_strerror(int status) {
         case DSV4_ERR_UNSUPPORTED: return "unsupported configuration";
         case DSV4_ERR_WORKSPACE: return "workspace too small";
         case DSV4_ERR_CUDA: return "CUDA error";
+        case DSV4_ERR_SCRATCH_LIMIT: return "call needs more scratch than the library's built-in buffer";
         default: return "unknown status";
     }
 }

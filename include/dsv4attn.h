@@ -84,6 +84,8 @@ extern "C" {
 #define DSV4_ERR_UNSUPPORTED  (-2)  /* page_size != 256, ratio not 0/4/128, row_bytes mis-sized */
 #define DSV4_ERR_WORKSPACE    (-3)  /* workspace smaller than dsv4_attn_workspace_size() */
 #define DSV4_ERR_CUDA         (-4)  /* a CUDA runtime call or launch failed */
+#define DSV4_ERR_SCRATCH_LIMIT (-5) /* dsv4_attn_c4_sparse_noalloc: the call needs more scratch than
+                                       the library's built-in DSV4_NOALLOC_SCRATCH_BYTES */
 
 /* ---- device error bits (dsv4_attn_get_device_error) ---- */
 #define DSV4_DEV_ERR_SWA_PAGE     0x01u  /* window row on a page id outside the SWA pool */
@@ -166,6 +168,36 @@ int dsv4_attn_verify(const void* q, int32_t num_tokens, int32_t batch, int32_t n
                      void* out, float* lse,
                      int32_t num_splits, void* workspace, size_t workspace_bytes,
                      int32_t* debug_rows, void* stream);
+
+/* Same computation, arguments and results as dsv4_attn_c4_sparse, for callers
+   that cannot allocate device memory themselves: code running where no
+   allocator may be called (inside another library's hot loop, in a process
+   whose memory is fully reserved up front, or from a runtime that only hands
+   out pointers it owns).  There is no workspace argument: the scratch the
+   split merge needs comes from a buffer inside this library, a static device
+   array of DSV4_NOALLOC_SCRATCH_BYTES that every GPU which loads the library
+   holds until the process exits.  This entry point has no counterpart on the
+   source pages; it only changes where the scratch lives.
+   - The first call on a device looks up the buffer's device address (one
+     runtime query, no allocation); make that first call before any stream
+     capture on that device.
+   - Every call uses the same buffer: calls that can overlap on the GPU (on
+     different streams without ordering between them) race and corrupt each
+     other's results.  Nothing in the buffer needs to start at zero; each call
+     writes every scratch byte it later reads.
+   - A call whose split plan needs more than DSV4_NOALLOC_SCRATCH_BYTES returns
+     DSV4_ERR_SCRATCH_LIMIT and launches nothing (dsv4_attn_workspace_size with
+     the same shapes gives the amount a call needs).
+   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+#define DSV4_NOALLOC_SCRATCH_BYTES (16u << 20)
+int dsv4_attn_c4_sparse_noalloc(const void* q, int32_t batch, int32_t num_heads,
+                                const int32_t* seq_lens, const int32_t* req_pool_indices,
+                                const dsv4_kv_pool* swa, int32_t window,
+                                const dsv4_kv_pool* extra,
+                                const int32_t* topk_idx, int32_t topk,
+                                const float* sink, float scale,
+                                void* out, float* lse,
+                                int32_t num_splits, int32_t* debug_rows, void* stream);
 
 /* The split plan the library uses for these shapes on the current device
    (num_splits as passed to an entry point; 0 = automatic).  Writes the
