@@ -60,6 +60,10 @@ constexpr uint32_t kTmemS = 0;       // two 64-column score buffers
 constexpr uint32_t kTmemO = 128;     // O^T: 4 x 64 columns, value dim 128*m + lane
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// packed FP8 row: [448 e4m3 nope][64 bf16 rope][7 fp32 scales][pad], 608 bytes
+constexpr int kFp8NopeBytes = 448;
+constexpr int kFp8ScaleOff = 448 + 128;
+constexpr int kFp8RowBytes = 608;
 
 // ------------------------------------------------------------------ smem
 constexpr int kChunk = 64 * 128;               // 64 rows x 128 B: one 64-dim chunk
@@ -387,7 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 for (int u = 0; u < kPer; ++u) {
                     const int sl = ring_base + lt + u * kLoadThreads;
                     ring[sl - ring_base] = rows[u];
-                    if (rows[u] >= 0) prefetch_l2(slot_row_ptr(p, ti, sl, rows[u]), 1024);
+                    if (rows[u] >= 0)
+                        prefetch_l2(slot_row_ptr(p, ti, sl, rows[u]), KV_FORMAT == DSV4_KV_BF16 ? 1024 : kFp8RowBytes);
                 }
                 named_barrier_sync(1, kLoadThreads);
                 if (lt == 0 && ring_base == ti.slot_begin) DSV4_TR(3);
@@ -404,20 +409,74 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 if (lane == 0) mbar_arrive(bar(B_MASK_FULL + stage));
             }
             const uint32_t dst_stage = sKV + stage * kStageBytes;
+            if constexpr (KV_FORMAT == DSV4_KV_BF16) {
 #pragma unroll 4
-            for (int k = 0; k < kTileN / kLoadWarps; ++k) {
-                const int r = lw * (kTileN / kLoadWarps) + k;
-                const int slot = slot0 + r;
-                const int row = slot < ti.slot_end ? ring[slot - ring_base] : -1;
-                const uint8_t* src = row >= 0 ? slot_row_ptr(p, ti, slot, row) : p.swa_rows;
+                for (int k = 0; k < kTileN / kLoadWarps; ++k) {
+                    const int r = lw * (kTileN / kLoadWarps) + k;
+                    const int slot = slot0 + r;
+                    const int row = slot < ti.slot_end ? ring[slot - ring_base] : -1;
+                    const uint8_t* src = row >= 0 ? slot_row_ptr(p, ti, slot, row) : p.swa_rows;
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int piece = lane + 32 * h2;       // 16-byte piece of the 1 KB row
-                    const uint32_t dst = dst_stage + (piece >> 3) * kChunk + sw128(r, piece & 7);
-                    cp_async_16(dst, src + (row >= 0 ? piece * 16 : 0), row >= 0 ? 16u : 0u);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int piece = lane + 32 * h2;       // 16-byte piece of the 1 KB row
+                        const uint32_t dst = dst_stage + (piece >> 3) * kChunk + sw128(r, piece & 7);
+                        cp_async_16(dst, src + (row >= 0 ? piece * 16 : 0), row >= 0 ? 16u : 0u);
+                    }
                 }
+                cp_async_arrive_noinc(bar(B_KV_FULL + stage));
+            } else {
+                // packed FP8 rows: lane l < 28 dequantises nope dims 16l..16l+15
+                // (e4m3 x the fp32 scale of their 64-dim block, rounded to bf16);
+                // lanes 28..31 copy 16 dims of the bf16 rope each.  The rows were
+                // prefetched into L2 when their slots were resolved.
+                constexpr int kR = kTileN / kLoadWarps;
+                uint4 raw[kR], raw2[kR];
+                float scl[kR];
+#pragma unroll
+                for (int k = 0; k < kR; ++k) {
+                    const int r = lw * kR + k;
+                    const int slot = slot0 + r;
+                    const int row = slot < ti.slot_end ? ring[slot - ring_base] : -1;
+                    raw[k] = raw2[k] = make_uint4(0, 0, 0, 0);
+                    scl[k] = 0.f;
+                    if (row >= 0) {
+                        const uint8_t* src = slot_row_ptr(p, ti, slot, row);
+                        if (lane < 28) {
+                            raw[k] = __ldg(reinterpret_cast<const uint4*>(src + lane * 16));
+                            scl[k] = __ldg(reinterpret_cast<const float*>(src + kFp8ScaleOff) + (lane >> 2));
+                        } else {
+                            const uint4* rp = reinterpret_cast<const uint4*>(src + kFp8NopeBytes + (lane - 28) * 32);
+                            raw[k] = __ldg(rp);
+                            raw2[k] = __ldg(rp + 1);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kR; ++k) {
+                    const int r = lw * kR + k;
+                    if (lane < 28) {
+                        const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+                        uint32_t o[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float f[4];
+                            e4m3x4_to_f32(w[e], f);
+                            o[2 * e] = pack_bf16x2(f[0] * scl[k], f[1] * scl[k]);
+                            o[2 * e + 1] = pack_bf16x2(f[2] * scl[k], f[3] * scl[k]);
+                        }
+                        const uint32_t cbase = dst_stage + (lane >> 2) * kChunk;
+                        st_shared_v4(cbase + sw128(r, 2 * (lane & 3)), o[0], o[1], o[2], o[3]);
+                        st_shared_v4(cbase + sw128(r, 2 * (lane & 3) + 1), o[4], o[5], o[6], o[7]);
+                    } else {
+                        const uint32_t cbase = dst_stage + 7 * kChunk;
+                        const int j = 2 * (lane - 28);
+                        st_shared_v4(cbase + sw128(r, j), raw[k].x, raw[k].y, raw[k].z, raw[k].w);
+                        st_shared_v4(cbase + sw128(r, j + 1), raw2[k].x, raw2[k].y, raw2[k].z, raw2[k].w);
+                    }
+                }
+                fence_proxy_async();
+                mbar_arrive(bar(B_KV_FULL + stage));
             }
-            cp_async_arrive_noinc(bar(B_KV_FULL + stage));
             if (lt == 0 && i < 8) DSV4_TR(4 + i);
         }
         cp_async_wait_all();
@@ -802,6 +861,9 @@ static int device_info(DeviceInfo& out) {
         auto kern = dsv4_attn_kernel<DSV4_KV_BF16>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) != cudaSuccess)
             return DSV4_ERR_CUDA;
+        if (cudaFuncSetAttribute(dsv4_attn_kernel<DSV4_KV_FP8_PACKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemAlloc) != cudaSuccess)
+            return DSV4_ERR_CUDA;
         for (int cl = 1; cl <= kMaxCluster; ++cl) {
             cudaLaunchConfig_t cfg = {};
             cudaLaunchAttribute attr[1];
@@ -869,6 +931,8 @@ static int check_pool(const dsv4_kv_pool* pool) {
     if (pool->page_size != kPageSize) return DSV4_ERR_UNSUPPORTED;
     if (pool->format == DSV4_KV_BF16) {
         if (pool->row_bytes != 1024) return DSV4_ERR_UNSUPPORTED;
+    } else if (pool->format == DSV4_KV_FP8_PACKED) {
+        if (pool->row_bytes != kFp8RowBytes) return DSV4_ERR_UNSUPPORTED;
     } else {
         return DSV4_ERR_UNSUPPORTED;
     }
@@ -1006,7 +1070,10 @@ static int run(const Call& c) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, dsv4_attn_kernel<DSV4_KV_BF16>, p) != cudaSuccess) {
+    const cudaError_t le = c.swa->format == DSV4_KV_BF16
+                               ? cudaLaunchKernelEx(&cfg, dsv4_attn_kernel<DSV4_KV_BF16>, p)
+                               : cudaLaunchKernelEx(&cfg, dsv4_attn_kernel<DSV4_KV_FP8_PACKED>, p);
+    if (le != cudaSuccess) {
         cudaGetLastError();
         return DSV4_ERR_CUDA;
     }

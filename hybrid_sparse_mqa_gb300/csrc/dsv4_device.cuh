@@ -4,6 +4,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace dsv4 {
 
@@ -230,6 +231,19 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Four OCP e4m3 codes (bytes of `w`, lowest first) -> float, exactly (every
+// e4m3 value is representable in f16).
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float (&f)[4]) {
+    uint32_t h01, h23;
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n"
+        " cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}\n"
+        : "=r"(h01), "=r"(h23)
+        : "r"(w));
+    const float2 a = __half22float2(*reinterpret_cast<__half2*>(&h01));
+    const float2 b = __half22float2(*reinterpret_cast<__half2*>(&h23));
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

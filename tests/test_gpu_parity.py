@@ -148,3 +148,18 @@ def test_device_errors_are_flagged_not_trapped(attn):
 def test_full_size_sampled(attn, name, tokens):
     inp = synth.make_inputs(name, device="cuda")
     run_and_compare(attn, inp, tokens=tokens)
+
+
+# ---------------------------------------------------------------- packed FP8 KV
+@pytest.mark.parametrize("kind,qlen", [("swa", 1), ("c4", 1), ("c128", 1), ("c4", 4), ("c128", 3)])
+def test_fp8_small(attn, kind, qlen):
+    run_and_compare(attn, small(kind, 64, (300, 1029, 5000), qlen=qlen, kv_format="fp8", seed=80))
+
+
+def test_fp8_h128(attn):
+    run_and_compare(attn, small("c128", 128, (700, 3000), kv_format="fp8", seed=81))
+
+
+def test_full_size_c4_verify_fp8_sampled(attn):
+    inp = synth.make_inputs("c4_verify_fp8", device="cuda")
+    run_and_compare(attn, inp, tokens=[0, 3, 130, 255])
