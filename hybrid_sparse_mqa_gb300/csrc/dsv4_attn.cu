@@ -110,9 +110,15 @@ __device__ unsigned int g_dev_error;
 constexpr int kTraceSlots = 64;
 constexpr int kTraceCtas = 2048;
 __device__ unsigned long long g_trace[kTraceCtas * kTraceSlots];
+// slots hold clock64() (SM cycles); slot 62 / 63 hold globaltimer at the first
+// and last mark of slot 0 / 57 so cycles can be converted to time per CTA
 __device__ __forceinline__ void trace_mark(int slot) {
     const int cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-    if (cta < kTraceCtas && slot < kTraceSlots) g_trace[cta * kTraceSlots + slot] = globaltimer_ns();
+    if (cta < kTraceCtas && slot < kTraceSlots) {
+        g_trace[cta * kTraceSlots + slot] = static_cast<unsigned long long>(clock64());
+        if (slot == 0) g_trace[cta * kTraceSlots + 62] = globaltimer_ns();
+        if (slot == 57) g_trace[cta * kTraceSlots + 63] = globaltimer_ns();
+    }
 }
 #define DSV4_TR(slot) trace_mark(slot)
 #else
