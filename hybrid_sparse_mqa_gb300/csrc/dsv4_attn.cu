@@ -11,15 +11,19 @@
 //   combine kernel.  With H = 128 the two head groups of a slice read the
 //   same rows.
 // * Per 64-key tile: eight loader warps resolve key slots to pool rows (SWA
-//   page table, C4 index list, C128 range), prefetch the rows into L2 as soon
-//   as they are resolved, and gather the 1 KB rows with 16-byte cp.async into
-//   a 128-byte-swizzled shared tile.  The MMA warp computes S = Q K^T on
-//   tcgen05 (M = 64 heads, N = 64 keys, K = 512; fp32 in TMEM).  Thread h of
-//   the four softmax warps owns head h's row of S: online softmax with a
-//   lazily updated running max, bf16 probabilities written as one 128-byte
-//   line.  The MMA warp then accumulates O^T += V^T P^T (M = 128 of the 512
-//   value dims per MMA, N = 64 heads, K = 64 keys) into 4 x 64 TMEM columns;
-//   V is the same shared tile read MN-major (K and V are the same row).
+//   page table, C4 index list, C128 range) one 256-slot chunk ahead of use and
+//   gather the 1 KB rows with 16-byte cp.async into a 128-byte-swizzled shared
+//   tile.  One MMA warp computes S = Q K^T on tcgen05 (M = 64 heads, N = 64
+//   keys, K = 512; fp32 in TMEM).  Four softmax warps read S with the 16-lane
+//   TMEM access shape: the two threads t and t ^ 2 hold the even and odd key
+//   columns of one head, so the online softmax (lazily updated running max,
+//   fp32 denominator) needs one shuffle per reduction; the bf16
+//   probabilities go into the head's 128-byte line.  A second MMA warp
+//   accumulates O^T += V^T P^T (M = 128 of the 512 value dims per MMA, N = 64
+//   heads, K = 64 keys) into 4 x 64 TMEM columns; V is the same shared tile
+//   read MN-major (K and V are the same row).  Each tcgen05.mma costs its
+//   issuing thread about as long as a small MMA takes to run, so the two
+//   products are issued from two warps and overlap.
 // * At the end the sink adds exp(sink - M) to each head's denominator, the
 //   slices are merged with log-sum-exp weights and the bf16 output written.
 //
@@ -46,12 +50,14 @@ constexpr int kPageSize = 256;
 constexpr int kTileN = 64;           // keys per tile
 constexpr int kStages = 2;           // gather pipeline depth (64 KB each)
 constexpr int kHG = 64;              // heads per CTA (MMA M of S = Q K^T)
-constexpr int kRing = 512;           // resolved key slots held at a time
+constexpr int kRingHalf = 256;       // key slots resolved per chunk (two chunks held)
+constexpr int kRing = 2 * kRingHalf;
 constexpr int kSoftmaxWarps = 4;
 constexpr int kLoadWarps = 8;
 constexpr int kLoadThreads = kLoadWarps * 32;
-constexpr int kMmaWarp = kSoftmaxWarps + kLoadWarps;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kQkWarp = kSoftmaxWarps + kLoadWarps;   // issues S = Q K^T (and owns the TMEM allocation)
+constexpr int kPvWarp = kQkWarp + 1;                  // issues O^T += V^T P^T
+constexpr int kThreads = (kPvWarp + 1) * 32;
 constexpr int kMaxCluster = 8;
 constexpr float kRescaleLog2 = 8.0f; // lazy rescale threshold (factor 256)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -76,7 +82,8 @@ constexpr int OFF_P = OFF_KV + kStages * kStageBytes;
 constexpr int OFF_RING = OFF_P + 2 * kPBytes;  // int32 pool rows of resolved slots
 constexpr int OFF_ML = OFF_RING + kRing * 4;   // float2 (m, l) per head
 constexpr int OFF_W = OFF_ML + kHG * 8;        // float per head: rescale / merge weights
-constexpr int OFF_MASK = OFF_W + kHG * 4;      // 64-bit key validity mask per stage
+constexpr int OFF_MLX = OFF_W + kHG * 4;       // float2 [slice][head]: every slice's (m, l), pushed by the slices
+constexpr int OFF_MASK = OFF_MLX + kMaxCluster * kHG * 8;   // 64-bit key validity mask per stage
 constexpr int OFF_BAR = OFF_MASK + kStages * 8;
 enum Bar {
     B_Q_FULL = 0,
@@ -92,14 +99,18 @@ enum Bar {
     B_COUNT
 };
 constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;
-constexpr int OFF_MERGE = OFF_KV;              // [owned dim][64 heads] fp32, reuses the KV stages
-                                               // (peers' bf16 blocks are staged in the Q area)
+constexpr int OFF_MERGE = OFF_KV;              // [owned dim][64 heads] fp32, reuses the KV stages,
+                                               // followed by the outgoing bf16 rows of the other dims;
+                                               // peers' bf16 blocks are staged in the Q area
 constexpr int kSmemUsed = OFF_MISC + 16;
 constexpr int kSmemAlloc = kSmemUsed + 1024;   // room to align the base to 1024 bytes
 static_assert(OFF_MERGE + kDim * kHG * 4 <= OFF_P, "merge buffer must fit in the KV stages");
+static_assert(kStages * kStageBytes >= kDim * kHG * 4, "owned fp32 rows + outgoing bf16 rows fit in the KV stages");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
-static_assert(kRing % kLoadThreads == 0, "ring slots per loader thread");
+static_assert(kRingHalf == kLoadThreads, "one slot per loader thread per chunk");
+static_assert(kRingHalf % kTileN == 0 && kRingHalf / kTileN == 4, "four tiles per ring chunk");
 static_assert(6 * 80 * 128 <= kQBytes, "staged peer blocks (at most 6 x 80 dims, Sc = 7) must fit in the Q area");
+static_assert(7 * 64 * 128 <= kQBytes, "staged peer blocks (7 x 64 dims, Sc = 8) must fit in the Q area");
 static_assert(kMaxCluster * kHG * 4 <= kRing * 4, "merge weights must fit in the ring");
 
 __device__ unsigned int g_dev_error;
@@ -185,11 +196,14 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int* abo
 }
 
 // Query token t -> request row, position and key-list extent of slice `split`.
+// In decode the request row does not depend on the position, so its load is
+// issued together with the sequence length.
 __device__ void token_info(const Params& p, int t, int split, TokenInfo& ti, unsigned& err) {
-    int b, pos;
+    int b, pos, trow;
     bool ok = true;
     if (p.cu_seqlens == nullptr) {
         b = t;
+        trow = p.rpi ? __ldg(p.rpi + b) : b;
         pos = __ldg(p.seq_lens + b) - 1;
     } else {
         int lo = 0, hi = p.batch - 1;        // largest b with cu[b] <= t
@@ -198,6 +212,7 @@ __device__ void token_info(const Params& p, int t, int split, TokenInfo& ti, uns
             if (__ldg(p.cu_seqlens + mid) <= t) lo = mid; else hi = mid - 1;
         }
         b = lo;
+        trow = p.rpi ? __ldg(p.rpi + b) : b;
         const int c0 = __ldg(p.cu_seqlens + b), c1 = __ldg(p.cu_seqlens + b + 1);
         if (t < c0 || t >= c1) ok = false;
         pos = __ldg(p.seq_lens + b) - (c1 - c0) + (t - c0);
@@ -206,7 +221,6 @@ __device__ void token_info(const Params& p, int t, int split, TokenInfo& ti, uns
         err |= DSV4_DEV_ERR_POSITION;
         ok = false;
     }
-    int trow = p.rpi ? __ldg(p.rpi + b) : b;
     if (ok && (trow < 0 || trow >= p.swa_pt_rows || (p.ratio != 0 && trow >= p.ex_pt_rows))) {
         err |= DSV4_DEV_ERR_REQ_ROW;
         ok = false;
@@ -227,11 +241,19 @@ __device__ void token_info(const Params& p, int t, int split, TokenInfo& ti, uns
     ti.ntiles = ti.slot_end > ti.slot_begin ? (ti.slot_end - ti.slot_begin + kTileN - 1) / kTileN : 0;
 }
 
+// C4 index of key slot `slot` (extra slots only).  With `has_spec`, `spec`
+// holds the index loaded for slot - window before the position was known,
+// which is the right one whenever the whole window is present.
+__device__ __forceinline__ int c4_index(const Params& p, int t, const TokenInfo& ti, int slot, bool has_spec,
+                                        int spec) {
+    return has_spec && ti.n_swa == p.window ? spec : __ldg(p.topk_idx + (size_t)t * p.topk + (slot - ti.n_swa));
+}
+
 // Key slot -> physical pool row (-1 = skipped).  Window slots are positions
 // pos-n_swa+1 .. pos in the SWA pool; extra slots are C4 indices or C128
-// compressed-row numbers in the extra pool.
-__device__ __forceinline__ int resolve_slot(const Params& p, int t, const TokenInfo& ti, int slot,
-                                            unsigned& err) {
+// compressed-row numbers in the extra pool.  `idx` is the slot's C4 index.
+__device__ __forceinline__ int resolve_slot_idx(const Params& p, const TokenInfo& ti, int slot, int idx,
+                                                unsigned& err) {
     if (slot < ti.n_swa) {
         const int j = ti.pos - ti.n_swa + 1 + slot;
         const int lp = j / kPageSize;
@@ -240,20 +262,22 @@ __device__ __forceinline__ int resolve_slot(const Params& p, int t, const TokenI
         if (page < 0 || page >= p.swa_pages) { err |= DSV4_DEV_ERR_SWA_PAGE; return -1; }
         return page * kPageSize + (j % kPageSize);
     }
-    const int e = slot - ti.n_swa;
-    int idx;
     if (p.ratio == 4) {
-        idx = __ldg(p.topk_idx + (size_t)t * p.topk + e);
         if (idx < 0) return -1;
         if (idx >= ti.n_c) { err |= DSV4_DEV_ERR_INDEX_RANGE; return -1; }
     } else {
-        idx = e;
+        idx = slot - ti.n_swa;
     }
     const int lp = idx / kPageSize;
     if (lp >= p.ex_pt_stride) { err |= DSV4_DEV_ERR_EXTRA_PAGE; return -1; }
     const int page = __ldg(p.ex_pt + (size_t)ti.trow * p.ex_pt_stride + lp);
     if (page < 0 || page >= p.ex_pages) { err |= DSV4_DEV_ERR_EXTRA_PAGE; return -1; }
     return page * kPageSize + (idx % kPageSize);
+}
+
+__device__ __forceinline__ int resolve_slot(const Params& p, int t, const TokenInfo& ti, int slot, unsigned& err) {
+    const int idx = (p.ratio == 4 && slot >= ti.n_swa) ? __ldg(p.topk_idx + (size_t)t * p.topk + (slot - ti.n_swa)) : 0;
+    return resolve_slot_idx(p, ti, slot, idx, err);
 }
 
 __device__ __forceinline__ const uint8_t* slot_row_ptr(const Params& p, const TokenInfo& ti, int slot, int row) {
@@ -311,6 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     const int split = gsplit * Sc + cs;
     const int head0 = grp * kHG;
     const int hcount = min(kHG, p.H - head0);
+    const bool is_loader = warp >= kSoftmaxWarps && warp < kQkWarp;
+    const int lt = tid - kSoftmaxWarps * 32;           // loader thread (when is_loader)
 
     const uint32_t sQ = base + OFF_Q, sKV = base + OFF_KV, sP = base + OFF_P;
     int* ring = reinterpret_cast<int*>(smem + OFF_RING);
@@ -324,8 +350,19 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
 
     unsigned err = 0;
     if (tid == 0) DSV4_TR(0);
+    // the merge-weight threads (warps 0..3, lanes 0..15: head 16 * warp + lane)
+    // fetch their head's sink logit now, off the epilogue's critical path
+    float sink_l2 = -INFINITY;
+    if (warp < 4 && lane < 16 && 16 * warp + lane < hcount) sink_l2 = __ldg(p.sink + head0 + 16 * warp + lane) * kLog2e;
 
     // ------------------------------------------------------------ set-up
+    // C4: each loader thread fetches the index of its first-chunk slot before
+    // the token's position is known, assuming the whole window is present
+    int idx_spec = -1;
+    if (is_loader && p.ratio == 4) {
+        const int e = split * p.chunk + lt - p.window;
+        if (e >= 0 && e < p.topk && lt < p.chunk) idx_spec = __ldg(p.topk_idx + (size_t)t * p.topk + e);
+    }
     if (tid == 0) {
         mbar_init(bar(B_Q_FULL), kSoftmaxWarps * 32);
         for (int s = 0; s < kStages; ++s) {
@@ -352,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         token_info(p, t, split, ti, e0);
         if (tid == 0) err |= e0;
     }
-    if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    if (warp == kQkWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -360,9 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     const int ntiles = ti.ntiles;
     if (tid == 0) DSV4_TR(1);
 
-    if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
+    if (is_loader) {
         // ============================================================ loader
-        const int lt = tid - kSoftmaxWarps * 32;
         const int lw = lt >> 5;
         if (p.debug_rows != nullptr && grp == 0) {
             const int d0 = split * p.chunk;
@@ -372,55 +408,39 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 p.debug_rows[(size_t)t * p.debug_stride + s] = row;
             }
         }
-        int ring_base = -1;
+        const int nslots = ti.slot_end - ti.slot_begin;
+        // chunk c of the slice (kRingHalf slots) goes to ring half c & 1
+        auto resolve_chunk = [&](int c) {
+            const int sl = ti.slot_begin + c * kRingHalf + lt;
+            int row = -1;
+            if (sl < ti.slot_end) {
+                const int idx = (p.ratio == 4 && sl >= ti.n_swa) ? c4_index(p, t, ti, sl, c == 0, idx_spec) : 0;
+                row = resolve_slot_idx(p, ti, sl, idx, err);
+            }
+            ring[(c & 1) * kRingHalf + lt] = row;
+        };
+        if (ntiles > 0) {
+            resolve_chunk(0);
+            named_barrier_sync(1, kLoadThreads);
+            if (lt == 0) DSV4_TR(3);
+        }
         for (int i = 0; i < ntiles; ++i) {
             const int stage = i & 1;
-            if (i >= kStages) {
-                wait_bar(bar(B_KV_EMPTY + stage), ((i >> 1) - 1) & 1, abort_flag);
-                fence_proxy_async();
-            }
+            const int c = i >> 2;
+            if ((i & 3) == 0 && i > 0) named_barrier_sync(1, kLoadThreads);   // chunk c resolved
             const int slot0 = ti.slot_begin + i * kTileN;
-            if (ring_base < 0 || slot0 + kTileN > ring_base + kRing) {
-                named_barrier_sync(1, kLoadThreads);
-                ring_base = slot0;
-                const int lim = min(ring_base + kRing, ti.slot_end);
-                // kRing / kLoadThreads slots per thread, their dependent loads in
-                // flight together; each resolved row is prefetched into L2
-                constexpr int kPer = kRing / kLoadThreads;
-                int rows[kPer];
-#pragma unroll
-                for (int u = 0; u < kPer; ++u) {
-                    const int sl = ring_base + lt + u * kLoadThreads;
-                    rows[u] = (sl < lim) ? resolve_slot(p, t, ti, sl, err) : -1;
-                }
-#pragma unroll
-                for (int u = 0; u < kPer; ++u) {
-                    const int sl = ring_base + lt + u * kLoadThreads;
-                    ring[sl - ring_base] = rows[u];
-                    if (rows[u] >= 0)
-                        prefetch_l2(slot_row_ptr(p, ti, sl, rows[u]), KV_FORMAT == DSV4_KV_BF16 ? 1024 : kFp8RowBytes);
-                }
-                named_barrier_sync(1, kLoadThreads);
-                if (lt == 0 && ring_base == ti.slot_begin) DSV4_TR(3);
-            }
-            {
-                // validity of the tile's 64 key slots, 8 per loader warp
-                constexpr int kRowsPerWarp = kTileN / kLoadWarps;
-                const int r = lw * kRowsPerWarp + (lane % kRowsPerWarp);
-                const int slot = slot0 + r;
-                const bool valid = slot < ti.slot_end && ring[slot - ring_base] >= 0;
-                const unsigned bal = __ballot_sync(0xffffffffu, lane < kRowsPerWarp && valid);
-                if (lane == 0) mask8[stage * kLoadWarps + lw] = static_cast<uint8_t>(bal & 0xffu);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_MASK_FULL + stage));
-            }
-            const uint32_t dst_stage = sKV + stage * kStageBytes;
+            const int* rg = ring + (c & 1) * kRingHalf + (i & 3) * kTileN;   // this tile's 64 rows
             if constexpr (KV_FORMAT == DSV4_KV_BF16) {
+                if (i >= kStages) {
+                    wait_bar(bar(B_KV_EMPTY + stage), ((i >> 1) - 1) & 1, abort_flag);
+                    fence_proxy_async();
+                }
+                const uint32_t dst_stage = sKV + stage * kStageBytes;
 #pragma unroll 4
                 for (int k = 0; k < kTileN / kLoadWarps; ++k) {
                     const int r = lw * (kTileN / kLoadWarps) + k;
                     const int slot = slot0 + r;
-                    const int row = slot < ti.slot_end ? ring[slot - ring_base] : -1;
+                    const int row = slot < ti.slot_end ? rg[r] : -1;
                     const uint8_t* src = row >= 0 ? slot_row_ptr(p, ti, slot, row) : p.swa_rows;
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
@@ -433,8 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             } else {
                 // packed FP8 rows: lane l < 28 dequantises nope dims 16l..16l+15
                 // (e4m3 x the fp32 scale of their 64-dim block, rounded to bf16);
-                // lanes 28..31 copy 16 dims of the bf16 rope each.  The rows were
-                // prefetched into L2 when their slots were resolved.
+                // lanes 28..31 copy 16 dims of the bf16 rope each.  The raw
+                // bytes are loaded before the stage is free.
                 constexpr int kR = kTileN / kLoadWarps;
                 uint4 raw[kR], raw2[kR];
                 float scl[kR];
@@ -442,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 for (int k = 0; k < kR; ++k) {
                     const int r = lw * kR + k;
                     const int slot = slot0 + r;
-                    const int row = slot < ti.slot_end ? ring[slot - ring_base] : -1;
+                    const int row = slot < ti.slot_end ? rg[r] : -1;
                     raw[k] = raw2[k] = make_uint4(0, 0, 0, 0);
                     scl[k] = 0.f;
                     if (row >= 0) {
@@ -457,6 +477,11 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                         }
                     }
                 }
+                if (i >= kStages) {
+                    wait_bar(bar(B_KV_EMPTY + stage), ((i >> 1) - 1) & 1, abort_flag);
+                    fence_proxy_async();
+                }
+                const uint32_t dst_stage = sKV + stage * kStageBytes;
 #pragma unroll
                 for (int k = 0; k < kR; ++k) {
                     const int r = lw * kR + k;
@@ -483,23 +508,56 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 fence_proxy_async();
                 mbar_arrive(bar(B_KV_FULL + stage));
             }
+            {
+                // validity of the tile's 64 key slots, 8 per loader warp
+                constexpr int kRowsPerWarp = kTileN / kLoadWarps;
+                const int r = lw * kRowsPerWarp + (lane % kRowsPerWarp);
+                const bool valid = slot0 + r < ti.slot_end && rg[r] >= 0;
+                const unsigned bal = __ballot_sync(0xffffffffu, lane < kRowsPerWarp && valid);
+                if (lane == 0) mask8[stage * kLoadWarps + lw] = static_cast<uint8_t>(bal & 0xffu);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_MASK_FULL + stage));
+            }
             if (lt == 0 && i < 8) DSV4_TR(4 + i);
+            // resolve the next chunk once this one's first two tiles are on their way
+            // (ring half (c + 1) & 1 was last read by chunk c - 1, finished by all)
+            if ((i & 3) == 1 && (c + 1) * kRingHalf < nslots) resolve_chunk(c + 1);
         }
         cp_async_wait_all();
-    } else if (warp == kMmaWarp) {
-        // ============================================================ MMA issuer
+    } else if (warp == kQkWarp) {
+        // ============================================================ S = Q K^T issuer
         if (lane == 0 && ntiles > 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kHG, kTileN, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kHG, true, false);
             wait_bar(bar(B_Q_FULL), 0, abort_flag);
             fence_proxy_async();
             tc_fence_after();
-            auto issue_pv = [&](int j) {
-                const int pb = j & 1;
-                const uint32_t stg = sKV + (j & 1) * kStageBytes;
-                wait_bar(bar(B_P_FULL + pb), (j >> 1) & 1, abort_flag);
-                if (j < 8) DSV4_TR(20 + j);
+            for (int i = 0; i < ntiles; ++i) {
+                wait_bar(bar(B_KV_FULL + (i & 1)), (i >> 1) & 1, abort_flag);
+                if (i >= 2) wait_bar(bar(B_S_FREE + (i & 1)), ((i - 2) >> 1) & 1, abort_flag);
+                if (i < 8) DSV4_TR(12 + i);
+                fence_proxy_async();
                 tc_fence_after();
+                const uint32_t stg = sKV + (i & 1) * kStageBytes;
+#pragma unroll
+                for (int k = 0; k < kDim / 16; ++k) {
+                    const uint64_t a = smem_desc_sw128(sQ + (k >> 2) * kChunk + (k & 3) * 32, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(stg + (k >> 2) * kChunk + (k & 3) * 32, 16, 1024);
+                    mma_bf16_ss(tmem + kTmemS + (i & 1) * kTileN, a, b, idesc_qk, k > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(B_S_FULL + (i & 1)));
+            }
+        }
+        __syncwarp();
+    } else if (warp == kPvWarp) {
+        // ============================================================ O^T += V^T P^T issuer
+        if (lane == 0 && ntiles > 0) {
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kHG, true, false);
+            for (int i = 0; i < ntiles; ++i) {
+                wait_bar(bar(B_P_FULL + (i & 1)), (i >> 1) & 1, abort_flag);
+                if (i < 8) DSV4_TR(20 + i);
+                tc_fence_after();
+                const uint32_t stg = sKV + (i & 1) * kStageBytes;
+                const uint32_t pbuf = sP + (i & 1) * kPBytes;
 #pragma unroll
                 for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
@@ -507,32 +565,13 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                         // A = V^T (dims 128*mt.., keys 16*kk..): MN-major, 64-dim atoms one chunk apart
                         const uint64_t a = smem_desc_sw128(stg + 2 * mt * kChunk + kk * 2048, kChunk, 1024);
                         // B = P (heads x keys), K-major
-                        const uint64_t b = smem_desc_sw128(sP + pb * kPBytes + kk * 32, 16, 1024);
-                        mma_bf16_ss(tmem + kTmemO + mt * kHG, a, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                        const uint64_t b = smem_desc_sw128(pbuf + kk * 32, 16, 1024);
+                        mma_bf16_ss(tmem + kTmemO + mt * kHG, a, b, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
-                mma_commit(bar(B_P_FREE + pb));
-                mma_commit(bar(B_KV_EMPTY + (j & 1)));
-            };
-            for (int i = 0; i < ntiles; ++i) {
-                const int stage = i & 1;
-                const int sb = i & 1;
-                wait_bar(bar(B_KV_FULL + stage), (i >> 1) & 1, abort_flag);
-                if (i < 8) DSV4_TR(12 + i);
-                fence_proxy_async();
-                if (i >= 2) wait_bar(bar(B_S_FREE + sb), ((i - 2) >> 1) & 1, abort_flag);
-                tc_fence_after();
-                const uint32_t stg = sKV + stage * kStageBytes;
-#pragma unroll
-                for (int k = 0; k < kDim / 16; ++k) {
-                    const uint64_t a = smem_desc_sw128(sQ + (k >> 2) * kChunk + (k & 3) * 32, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(stg + (k >> 2) * kChunk + (k & 3) * 32, 16, 1024);
-                    mma_bf16_ss(tmem + kTmemS + sb * kTileN, a, b, idesc_qk, k > 0 ? 1u : 0u);
-                }
-                mma_commit(bar(B_S_FULL + sb));
-                if (i >= 1) issue_pv(i - 1);
+                mma_commit(bar(B_P_FREE + (i & 1)));
+                mma_commit(bar(B_KV_EMPTY + (i & 1)));
             }
-            issue_pv(ntiles - 1);
             mma_commit(bar(B_O_FINAL));
         }
         __syncwarp();
@@ -549,60 +588,76 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             }
             cp_async_arrive_noinc(bar(B_Q_FULL));
         }
-        // head row h lives in TMEM lane 32*warp + (h % 16) for M = 64; lanes
-        // 16..31 of each warp hold no row but join every warp-wide TMEM access
-        const bool owner = lane < 16;
-        const int h = warp * 16 + (lane & 15);
-        const bool live = owner && h < hcount;
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        // Head row h of S lives in TMEM lane 32*(h / 16) + h % 16 (M = 64).  The
+        // 16x64b access shape gives thread t of warp h / 16 the columns of
+        // parity (t >> 1) & 1 of lane (t >> 2) + 8 * (t & 1): threads t and
+        // t ^ 2 share a head and hold its even and odd keys.
+        const int qd = warp;
+        const int par = (lane >> 1) & 1;
+        const int h = qd * 16 + (lane >> 2) + 8 * (lane & 1);
+        const bool live = h < hcount;
+        const bool owner = par == 0;                 // writes the head's per-head values
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(qd * 32) << 16);
         float m_run = -INFINITY, l_run = 0.f;
         for (int i = 0; i < ntiles; ++i) {
             const int sb = i & 1;
             const int stage = i & 1;
-            float s[64];
+            float s[32];
             wait_bar(bar(B_S_FULL + sb), (i >> 1) & 1, abort_flag);
             if (tid == 0 && i < 8) DSV4_TR(28 + i);
             __syncwarp();
             tc_fence_after();
-            {
-                float a[32], b[32];
-                tmem_ld32(lane_addr + kTmemS + sb * kTileN, a);
-                tmem_ld32(lane_addr + kTmemS + sb * kTileN + 32, b);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) { s[j] = a[j]; s[32 + j] = b[j]; }
-            }
+            tmem_ld16x64b_x32(lane_addr + kTmemS + sb * kTileN, s);
             tc_fence_before();
             mbar_arrive(bar(B_S_FREE + sb));
             wait_bar(bar(B_MASK_FULL + stage), (i >> 1) & 1, abort_flag);
-            const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + OFF_MASK + stage * 8);
-            float mt = -INFINITY;
+            const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + OFF_MASK + stage * 8) >> par;
+            float tmax = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                s[j] = ((mask >> j) & 1ull) ? s[j] * p.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, s[j]);
+            for (int j = 0; j < 32; ++j) {
+                s[j] = ((mask >> (2 * j)) & 1ull) ? s[j] * p.scale_log2 : -INFINITY;
+                tmax = fmaxf(tmax, s[j]);
             }
-            const bool need = live && mt > m_run + kRescaleLog2;
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+            const bool need = live && tmax > m_run + kRescaleLog2;
             float alpha = 1.f;
             if (need) {
-                alpha = fast_exp2(m_run - mt);
-                m_run = mt;
+                alpha = fast_exp2(m_run - tmax);
+                m_run = tmax;
             }
-            uint32_t pk[32];
+            float pv[32];
             float lsum = 0.f;
             const bool any = live && m_run != -INFINITY;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const float p0 = any ? fast_exp2(s[2 * j] - m_run) : 0.f;
-                const float p1 = any ? fast_exp2(s[2 * j + 1] - m_run) : 0.f;
                 // the denominator sums the fp32 probabilities; the bf16 copies
                 // only feed the PV product
-                lsum += p0 + p1;
-                pk[j] = pack_bf16x2(p0, p1);
+                pv[j] = any ? fast_exp2(s[j] - m_run) : 0.f;
+                lsum += pv[j];
             }
             l_run = l_run * alpha + lsum;
+            // bf16 words (key 2w, key 2w + 1) of the head's line: the even-key
+            // thread builds words 0..15, the odd-key thread words 16..31
+            uint32_t wd[16];
+            {
+                uint32_t snd[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    snd[m] = par ? pack_bf16x2(pv[2 * m], pv[2 * m + 1]) : pack_bf16x2(pv[16 + 2 * m], pv[17 + 2 * m]);
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const uint32_t rcv = __shfl_xor_sync(0xffffffffu, snd[m], 2);
+                    const uint32_t own = par ? pack_bf16x2(pv[16 + 2 * m], pv[17 + 2 * m]) : pack_bf16x2(pv[2 * m], pv[2 * m + 1]);
+                    // own / rcv hold keys of j = 2m and 2m + 1 (offset 16 for the odd thread)
+                    const uint32_t ev = par ? rcv : own;   // even keys (j = 2m, 2m + 1 of the word range)
+                    const uint32_t od = par ? own : rcv;   // odd keys
+                    wd[2 * m] = __byte_perm(ev, od, 0x5410);      // (even j=2m, odd j=2m)
+                    wd[2 * m + 1] = __byte_perm(ev, od, 0x7632);  // (even j=2m+1, odd j=2m+1)
+                }
+            }
             if (i > 0) {
                 // a head whose running max moved scales its O^T column; each
-                // softmax thread holds one value dim of O^T for all heads
+                // softmax warp scales the 32 value dims of its TMEM quadrant
                 if (bar_red_or(2, kSoftmaxWarps * 32, need)) {
                     if (owner) wsm[h] = alpha;
                     named_barrier_sync(2, kSoftmaxWarps * 32);
@@ -620,122 +675,182 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 }
             }
             if (i >= 2) wait_bar(bar(B_P_FREE + sb), ((i - 2) >> 1) & 1, abort_flag);
-            if (owner) {
+            {
                 const uint32_t prow = sP + sb * kPBytes;
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_shared_v4(prow + sw128(h, q), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                for (int q = 0; q < 4; ++q)
+                    st_shared_v4(prow + sw128(h, 4 * par + q), wd[4 * q], wd[4 * q + 1], wd[4 * q + 2], wd[4 * q + 3]);
             }
             fence_proxy_async();
             tc_fence_before();
             mbar_arrive(bar(B_P_FULL + sb));
             if (tid == 0 && i < 8) DSV4_TR(44 + i);
         }
+        // the head's denominator is the sum of its two halves; (m, l) goes to
+        // slot cs of every slice's table (its own included)
+        const float l_all = l_run + __shfl_xor_sync(0xffffffffu, l_run, 2);
+        if (owner) {
+            const float2 v = make_float2(live && ntiles > 0 ? m_run : -INFINITY, live && ntiles > 0 ? l_all : 0.f);
+            ml[h] = v;
+            const uint32_t dst = base + OFF_MLX + (cs * kHG + h) * 8;
+            for (int s2 = 0; s2 < Sc; ++s2) {
+                const uint32_t r = mapa(dst, static_cast<uint32_t>(s2 * G + grp));
+                asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(r), "f"(v.x), "f"(v.y) : "memory");
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ epilogue
+    // Slice cs owns the 8-dim units [u_lo, u_hi) of the output (nd dims from
+    // dbase).  Every thread that reads O^T holds one value dim for all heads:
+    // owned dims go to the fp32 rows T[dim][head]; the other dims go, as bf16
+    // rows, to the outgoing area (row order = dim order without the owned
+    // range, so each peer's dims are one contiguous block), from where one
+    // bulk copy per peer stores them to the workspace.  After the cluster
+    // barrier each slice bulk-loads its dims from every peer (L2 and bulk
+    // copies move these far faster than distributed shared memory does).
+    // Bf16 rows are 128 B with 16-byte chunk q stored at q ^ (dim & 7).
+    const int u_lo = (cs * 64) / Sc, u_hi = ((cs + 1) * 64) / Sc;
+    const int nd = 8 * (u_hi - u_lo), dbase = 8 * u_lo;
+    float* T = reinterpret_cast<float*>(smem + OFF_MERGE);
+    const uint32_t sOut = base + OFF_MERGE + nd * kHG * 4;           // outgoing bf16 rows
+    uint16_t* mrg_t = p.merge + (((size_t)t * p.gsplits + gsplit) * G + grp) * Sc * (kDim * kHG);
+    {
+        // ============================================================ O^T read-out
+        // (quadrant qd, value tile mt) jobs: warp w takes (w % 4, w / 4); warps
+        // 2 and 3 also take mt = 3 of their quadrants.
         if (ntiles > 0) {
             wait_bar(bar(B_O_FINAL), 0, abort_flag);
             if (tid == 0) DSV4_TR(52);
             tc_fence_after();
             fence_proxy_async();
+            if (tid == 0) DSV4_TR(53);
         }
-        if (owner) ml[h] = make_float2(live && ntiles > 0 ? m_run : -INFINITY, live && ntiles > 0 ? l_run : 0.f);
-        // Slice cs owns the 8-dim units [u_lo, u_hi) of the output.  Each
-        // softmax thread holds one value dim of this slice's (unnormalised)
-        // accumulator for all heads: owned dims go to the local fp32 buffer
-        // T[dim][head]; the others go (bf16) to the workspace, where their
-        // owners fetch them after the cluster barrier (L2 and bulk copies move
-        // these far faster than distributed shared memory does).
-        const int u_lo = (cs * 64) / Sc, u_hi = ((cs + 1) * 64) / Sc;
-        float* T = reinterpret_cast<float*>(smem + OFF_MERGE);
-        uint16_t* mrg_t = p.merge + (((size_t)t * p.gsplits + gsplit) * G + grp) * Sc * (kDim * kHG);
+        const int qd = warp & 3;
         __syncwarp();
-#pragma unroll 1
-        for (int mt = 0; mt < 4; ++mt) {
+        const int njobs = (warp == 2 || warp == 3) ? 2 : 1;
+        for (int jb = 0; jb < njobs; ++jb) {
+            const int mt = jb == 0 ? warp >> 2 : 3;
             float o[64];
             if (ntiles > 0) {
+                const uint32_t la = tmem + (static_cast<uint32_t>(qd * 32) << 16) + kTmemO + mt * kHG;
                 float a[32], b[32];
-                tmem_ld32(lane_addr + kTmemO + mt * kHG, a);
-                tmem_ld32(lane_addr + kTmemO + mt * kHG + 32, b);
+                tmem_ld32(la, a);
+                tmem_ld32(la + 32, b);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) { o[j] = a[j]; o[32 + j] = b[j]; }
+                if (tid == 0) DSV4_TR(54);
             } else {
 #pragma unroll
                 for (int j = 0; j < 64; ++j) o[j] = 0.f;
             }
-            const int d = mt * 128 + warp * 32 + lane;           // this thread's value dim
-            const int u = d >> 3;
-            if (u >= u_lo && u < u_hi) {
-                const int dl = d - 8 * u_lo;
+            const int d = mt * 128 + qd * 32 + lane;           // this thread's value dim
+            if (d >= dbase && d < dbase + nd) {
+                const int dl = d - dbase;
                 float* row = T + dl * kHG;
 #pragma unroll
                 for (int q = 0; q < 16; ++q)   // 16-byte chunk q of the row, swizzled by dim
                     *reinterpret_cast<float4*>(row + 4 * (q ^ (dl & 15))) =
                         make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
             } else {
-                uint4* dst = reinterpret_cast<uint4*>(mrg_t + ((size_t)cs * kDim + d) * kHG);
+                const int r = d < dbase ? d : d - nd;
+                const uint32_t row = sOut + r * 128;
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    dst[q] = make_uint4(pack_bf16x2(o[8 * q], o[8 * q + 1]), pack_bf16x2(o[8 * q + 2], o[8 * q + 3]),
-                                        pack_bf16x2(o[8 * q + 4], o[8 * q + 5]),
-                                        pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
+                    st_shared_v4(row + ((q ^ (d & 7)) << 4), pack_bf16x2(o[8 * q], o[8 * q + 1]),
+                                 pack_bf16x2(o[8 * q + 2], o[8 * q + 3]), pack_bf16x2(o[8 * q + 4], o[8 * q + 5]),
+                                 pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
+            }
+            if (Sc > 1) {
+                // the warp's 32 dims: the rows outside the owned range go to the
+                // workspace rows [cs][dim][head] (at most two runs of rows)
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    const int d0 = mt * 128 + qd * 32, d1 = d0 + 32;
+                    const int runs[2][2] = {{d0, min(d1, dbase)}, {max(d0, dbase + nd), d1}};
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int a0 = runs[k][0], a1 = runs[k][1];
+                        if (a0 >= a1) continue;
+                        const int r0 = a0 < dbase ? a0 : a0 - nd;
+                        uint16_t* dst = mrg_t + ((size_t)cs * kDim + a0) * kHG;
+                        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                                     "r"(sOut + r0 * 128), "r"(static_cast<uint32_t>((a1 - a0) * 128))
+                                     : "memory");
+                    }
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                }
+            }
+        }
+        if (Sc > 1 && lane == 0) {
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        __syncwarp();
+    }
+    if (tid == 0) DSV4_TR(60);
+    const bool final_out = p.gsplits == 1;
+    const uint32_t sIn = base + OFF_Q;                               // peers' bf16 rows [slot][dim]
+    float* W = reinterpret_cast<float*>(smem + OFF_RING);            // [slice][head] merge weights
+    const int issuer = kQkWarp * 32;
+    if (Sc > 1) {
+        tc_fence_before();
+        cluster_sync();   // B: every slice's rows and (m, l) are published
+        tc_fence_after();
+        if (tid == 0) DSV4_TR(55);
+        if (tid == issuer) {
+            // this slice's dims from every other slice: one contiguous block each
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            const uint32_t mb = bar(B_MERGE);
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb),
+                         "r"(static_cast<uint32_t>((Sc - 1) * nd * 128))
+                         : "memory");
+            int slot = 0;
+            for (int s2 = 0; s2 < Sc; ++s2) {
+                if (s2 == cs) continue;
+                const uint16_t* src = mrg_t + ((size_t)s2 * kDim + dbase) * kHG;
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                        sIn + slot * nd * 128),
+                    "l"(src), "r"(static_cast<uint32_t>(nd * 128)), "r"(mb)
+                    : "memory");
+                ++slot;
             }
         }
     }
-
-    // ------------------------------------------------------------ merge
-    if (tid == 0) DSV4_TR(60);
-    tc_fence_before();
-    cluster_sync();   // B: every slice's accumulator and (m, l) are published
-    tc_fence_after();
-    if (tid == 0) DSV4_TR(55);
-    const bool final_out = p.gsplits == 1;
-    const int u_lo = (cs * 64) / Sc, u_hi = ((cs + 1) * 64) / Sc;
-    const int nd = 8 * (u_hi - u_lo);                                // dims this slice owns
-    const int dmax = 8 * ((64 + Sc - 1) / Sc);
-    const float* T = reinterpret_cast<const float*>(smem + OFF_MERGE);
-    const uint8_t* stage_in = smem + OFF_Q;                          // peers' bf16 blocks [slot][dim][head]
-    float* W = reinterpret_cast<float*>(smem + OFF_RING);            // [slice][head] merge weights
-    const uint16_t* mrg_t = p.merge + (((size_t)t * p.gsplits + gsplit) * G + grp) * Sc * (kDim * kHG);
-    if (Sc > 1 && tid == kMmaWarp * 32) {
-        // fetch this slice's dims from every other slice: one contiguous block each
-        const uint32_t mb = bar(B_MERGE);
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb),
-                     "r"(static_cast<uint32_t>((Sc - 1) * nd * 128))
-                     : "memory");
-        int slot = 0;
-        for (int s2 = 0; s2 < Sc; ++s2) {
-            if (s2 == cs) continue;
-            const uint16_t* src = mrg_t + ((size_t)s2 * kDim + 8 * u_lo) * kHG;
-            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                             sQ + slot * dmax * 128),
-                         "l"(src), "r"(static_cast<uint32_t>(nd * 128)), "r"(mb)
-                         : "memory");
-            ++slot;
-        }
+    else {
+        __syncthreads();   // T complete
     }
-    if (warp < kSoftmaxWarps && lane < 16) {
+    const float2* mlx = reinterpret_cast<const float2*>(smem + OFF_MLX);
+    if (warp < 4 && lane < 16) {
         // weights of every slice's accumulator for head h: exp(m_s - M) / L
         const int h = warp * 16 + lane;
         const bool live = h < hcount;
+        if (tid == 0) DSV4_TR(36);
         float2 mls[kMaxCluster];
 #pragma unroll
         for (int s2 = 0; s2 < kMaxCluster; ++s2)
-            mls[s2] = s2 < Sc ? *cluster_ptr(&ml[h], s2 * G + grp) : make_float2(-INFINITY, 0.f);
+            mls[s2] = s2 < Sc ? (Sc > 1 ? mlx[s2 * kHG + h] : ml[h]) : make_float2(-INFINITY, 0.f);
         float M = -INFINITY;
 #pragma unroll
         for (int s2 = 0; s2 < kMaxCluster; ++s2) M = fmaxf(M, mls[s2].x);
-        const float sk = live ? __ldg(p.sink + head0 + h) * kLog2e : -INFINITY;
+        if (tid == 0) DSV4_TR(37);
+        const float sk = sink_l2;
         if (final_out) M = fmaxf(M, sk);
         float Lsum = 0.f;
-        if (M != -INFINITY) {
+        float e[kMaxCluster];
 #pragma unroll
-            for (int s2 = 0; s2 < kMaxCluster; ++s2)
-                if (mls[s2].x != -INFINITY) Lsum += mls[s2].y * exp2f(mls[s2].x - M);
-            if (final_out && sk != -INFINITY) Lsum += exp2f(sk - M);
+        for (int s2 = 0; s2 < kMaxCluster; ++s2) {
+            e[s2] = (M != -INFINITY && mls[s2].x != -INFINITY) ? fast_exp2(mls[s2].x - M) : 0.f;
+            Lsum += mls[s2].y * e[s2];
         }
+        if (final_out && M != -INFINITY && sk != -INFINITY) Lsum += fast_exp2(sk - M);
+        const float inv = (live && Lsum > 0.f) ? 1.f / Lsum : 0.f;
 #pragma unroll
         for (int s2 = 0; s2 < kMaxCluster; ++s2)
-            if (s2 < Sc)
-                W[s2 * kHG + h] = (live && Lsum > 0.f && mls[s2].x != -INFINITY) ? exp2f(mls[s2].x - M) / Lsum : 0.f;
+            if (s2 < Sc) W[s2 * kHG + h] = e[s2] * inv;
+        if (tid == 0) DSV4_TR(58);
         if (live && cs == 0) {
             if (final_out) {
                 if (p.lse) p.lse[(size_t)t * p.H + head0 + h] = (Lsum > 0.f ? M + log2f(Lsum) : -INFINITY) * kLn2;
@@ -745,61 +860,78 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         }
     }
     __syncthreads();
+    if (Sc > 1) wait_bar(bar(B_MERGE), 0, abort_flag);
+    if (tid == 0) DSV4_TR(59);
+    // output: items (owned dim, 16-head quarter), consecutive threads on
+    // consecutive dims so that every head's stores are contiguous
+    for (int it = tid; it < nd * 4; it += kThreads) {
+        const int dl = it % nd, hq = it / nd;
+        const int d = dbase + dl;
+        float acc[16];
+        {
+            const float* row = T + dl * kHG;
+            const float4* wown = reinterpret_cast<const float4*>(W + cs * kHG + 16 * hq);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = *reinterpret_cast<const float4*>(row + 4 * ((4 * hq + q) ^ (dl & 15)));
+                const float4 w = wown[q];
+                acc[4 * q] = w.x * v.x;
+                acc[4 * q + 1] = w.y * v.y;
+                acc[4 * q + 2] = w.z * v.z;
+                acc[4 * q + 3] = w.w * v.w;
+            }
+        }
+        int slot = 0;
+        for (int s2 = 0; s2 < Sc; ++s2) {
+            if (s2 == cs) continue;
+            const float4* ws = reinterpret_cast<const float4*>(W + s2 * kHG + 16 * hq);
+            const uint32_t row = sIn + (slot * nd + dl) * 128;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const float4 v = ld_shared_v4(row + (((2 * hq + q) ^ (d & 7)) << 4));
+                const uint32_t w4[4] = {__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                                        __float_as_uint(v.w)};
+                const float4 wa = ws[2 * q], wb = ws[2 * q + 1];
+                const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[8 * q + 2 * e] += wv[2 * e] * __uint_as_float(w4[e] << 16);
+                    acc[8 * q + 2 * e + 1] += wv[2 * e + 1] * __uint_as_float(w4[e] & 0xffff0000u);
+                }
+            }
+            ++slot;
+        }
+        const int h0 = 16 * hq;
+        if (final_out) {
+            __nv_bfloat16* o = p.out + ((size_t)t * p.H + head0 + h0) * kDim + d;
+#pragma unroll
+            for (int h = 0; h < 16; ++h)
+                if (h0 + h < hcount) o[(size_t)h * kDim] = __float2bfloat16_rn(acc[h]);
+        } else {
+            float* o = p.part_o + (((size_t)t * p.gsplits + gsplit) * p.H + head0 + h0) * kDim + d;
+#pragma unroll
+            for (int h = 0; h < 16; ++h)
+                if (h0 + h < hcount) o[(size_t)h * kDim] = acc[h];
+        }
+    }
+    if (tid == 0) DSV4_TR(61);
     if (Sc > 1) {
-        wait_bar(bar(B_MERGE), 0, abort_flag);
         // the workspace lines just copied are dead: drop them without write-back
         for (int ln = tid; ln < (Sc - 1) * nd; ln += kThreads) {
             int s2 = ln / nd;
             if (s2 >= cs) ++s2;
-            const uint16_t* lp = mrg_t + ((size_t)s2 * kDim + 8 * u_lo + ln % nd) * kHG;   // one 128-byte line
+            const uint16_t* lp = mrg_t + ((size_t)s2 * kDim + dbase + ln % nd) * kHG;   // one 128-byte line
             asm volatile("discard.global.L2 [%0], 128;" ::"l"(lp) : "memory");
-        }
-    }
-    if (tid == 0) DSV4_TR(59);
-    {
-        // output: item (head, 8 dims), consecutive threads on consecutive heads
-        const int items = hcount * (u_hi - u_lo);
-        for (int it = tid; it < items; it += kThreads) {
-            const int hh = it % hcount;
-            const int u = u_lo + it / hcount;
-            const int dl0 = 8 * (u - u_lo);
-            const float wown = W[cs * kHG + hh];
-            float acc[8];
-#pragma unroll
-            for (int k2 = 0; k2 < 8; ++k2) {
-                const int dl = dl0 + k2;
-                acc[k2] = wown * T[dl * kHG + 4 * ((hh >> 2) ^ (dl & 15)) + (hh & 3)];
-            }
-            int slot = 0;
-            for (int s2 = 0; s2 < Sc; ++s2) {
-                if (s2 == cs) continue;
-                const float ws = W[s2 * kHG + hh];
-                const uint16_t* blk = reinterpret_cast<const uint16_t*>(stage_in + slot * dmax * 128);
-#pragma unroll
-                for (int k2 = 0; k2 < 8; ++k2)
-                    acc[k2] += ws * __uint_as_float(static_cast<uint32_t>(blk[(dl0 + k2) * kHG + hh]) << 16);
-                ++slot;
-            }
-            const size_t rowoff = ((size_t)t * p.H + head0 + hh) * kDim + u * 8;
-            if (final_out) {
-                uint4 v;
-                v.x = pack_bf16x2(acc[0], acc[1]);
-                v.y = pack_bf16x2(acc[2], acc[3]);
-                v.z = pack_bf16x2(acc[4], acc[5]);
-                v.w = pack_bf16x2(acc[6], acc[7]);
-                *reinterpret_cast<uint4*>(p.out + rowoff) = v;
-            } else {
-                float* dst = p.part_o + (((size_t)t * p.gsplits + gsplit) * p.H + head0 + hh) * kDim + u * 8;
-                *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-            }
         }
     }
     if (err) atomicOr(&g_dev_error, err);
     if (tid == 0) DSV4_TR(56);
-    cluster_sync();   // C: peers are done reading this CTA's shared memory
+    // no slice touches another's shared memory after barrier B
+    tc_fence_before();
+    __syncthreads();
     if (tid == 0) DSV4_TR(57);
-    if (warp == kMmaWarp) {
+    if (warp == kQkWarp) {
+        tc_fence_after();
         if (*reinterpret_cast<volatile int*>(abort_flag)) {
             // a wait gave up: give in-flight tensor-core work time to drain
             for (int k = 0; k < 1000; ++k) __nanosleep(10000);
@@ -812,8 +944,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
 // L_g * exp(M_g - M) with M the largest of the M_g and the sink; the sink
 // adds exp(sink - M) to the denominator and nothing to the numerator.
 __global__ void __launch_bounds__(256) dsv4_combine_kernel(const __grid_constant__ Params p) {
-    const int t = blockIdx.x;
-    for (int it = threadIdx.x; it < p.H * 64; it += blockDim.x) {
+    const int t = blockIdx.y;
+    {
+        const int it = blockIdx.x * blockDim.x + threadIdx.x;   // (head, 8-dim unit)
+        if (it >= p.H * 64) return;
         const int h = it >> 6;
         const int u = it & 63;
         const float sk = __ldg(p.sink + h) * kLog2e;
@@ -901,8 +1035,10 @@ static int list_max(int ratio, int window, int topk, int max_seq_len) {
 }
 
 // Split plan: Sc key slices merged inside the kernel (one cluster of Sc x G
-// CTAs, G head groups) times Sg cluster groups merged by the combine kernel,
-// chosen to minimise waves x tiles per slice.
+// CTAs, G head groups) times Sg cluster groups merged by the combine kernel.
+// Cost in units of one 64-key tile: each wave of CTAs pays its slice's tiles
+// plus a fixed start-up and epilogue cost; the combine kernel and every extra
+// in-cluster slice add their merge work.
 static int make_plan(int T, int G, int lmax, int num_splits, const DeviceInfo& di, int& sc, int& sg) {
     const int tiles_total = (lmax + kTileN - 1) / kTileN;
     const int max_sc = kMaxCluster / G;
@@ -925,7 +1061,7 @@ static int make_plan(int T, int G, int lmax, int num_splits, const DeviceInfo& d
             if (g > 1 && clusters > 4LL * per_wave) break;
             const long long waves = (clusters + per_wave - 1) / per_wave;
             const double tiles = (double)lmax / s / kTileN;
-            const double cost = (double)waves * (tiles + 1.5) + (g > 1 ? 3.0 : 0.0) + 0.5 * (c - 1);
+            const double cost = (double)waves * (tiles + 3.0) + (g > 1 ? 4.0 : 0.0) + 0.5 * (c - 1);
             if (cost < best - 1e-9) { best = cost; sc = c; sg = g; }
         }
     }
@@ -1084,7 +1220,7 @@ static int run(const Call& c) {
         return DSV4_ERR_CUDA;
     }
     if (sg > 1) {
-        dsv4_combine_kernel<<<c.T, 256, 0, st>>>(p);
+        dsv4_combine_kernel<<<dim3((c.H * 64 + 255) / 256, c.T), 256, 0, st>>>(p);
         if (cudaGetLastError() != cudaSuccess) return DSV4_ERR_CUDA;
     }
     return DSV4_OK;
