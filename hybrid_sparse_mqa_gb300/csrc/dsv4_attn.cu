@@ -47,23 +47,24 @@ namespace dsv4 {
 // ------------------------------------------------------------------ shape
 constexpr int kDim = 512;
 constexpr int kPageSize = 256;
-constexpr int kTileN = 64;           // keys per tile
-constexpr int kStages = 2;           // gather pipeline depth (64 KB each)
+constexpr int kTileN = 48;           // keys per tile
+constexpr int kStages = 3;           // gather pipeline depth (48 KB each)
 constexpr int kHG = 64;              // heads per CTA (MMA M of S = Q K^T)
-constexpr int kRingHalf = 256;       // key slots resolved per chunk (two chunks held)
+constexpr int kRingHalf = 192;       // key slots resolved per chunk (four tiles; two chunks held)
 constexpr int kRing = 2 * kRingHalf;
 constexpr int kSoftmaxWarps = 4;
 constexpr int kLoadWarps = 8;
 constexpr int kLoadThreads = kLoadWarps * 32;
-constexpr int kQkWarp = kSoftmaxWarps + kLoadWarps;   // issues S = Q K^T (and owns the TMEM allocation)
-constexpr int kPvWarp = kQkWarp + 1;                  // issues O^T += V^T P^T
+constexpr int kQkWarp = kSoftmaxWarps + kLoadWarps;   // S = Q K^T over dims 0..255 (owns the TMEM allocation);
+                                                      // warp kQkWarp + 1 takes dims 256..511
+constexpr int kPvWarp = kQkWarp + 2;                  // issues O^T += V^T P^T
 constexpr int kThreads = (kPvWarp + 1) * 32;
 constexpr int kMaxCluster = 8;
 constexpr float kRescaleLog2 = 8.0f; // lazy rescale threshold (factor 256)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;       // two 64-column score buffers
-constexpr uint32_t kTmemO = 128;     // O^T: 4 x 64 columns, value dim 128*m + lane
+constexpr uint32_t kTmemS = 0;       // score halves: buffer b, dim half d at column 96 b + 48 d
+constexpr uint32_t kTmemO = 256;     // O^T: 4 x 64 columns, value dim 128*m + lane
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // packed FP8 row: [448 e4m3 nope][64 bf16 rope][7 fp32 scales][pad], 608 bytes
@@ -72,18 +73,18 @@ constexpr int kFp8ScaleOff = 448 + 128;
 constexpr int kFp8RowBytes = 608;
 
 // ------------------------------------------------------------------ smem
-constexpr int kChunk = 64 * 128;               // 64 rows x 128 B: one 64-dim chunk
-constexpr int kQBytes = 8 * kChunk;            // 64 heads x 512 dims
-constexpr int kStageBytes = 8 * kChunk;        // 64 keys x 512 dims
-constexpr int kPBytes = kHG * 128;             // 64 heads x 64 keys bf16
+constexpr int kChunkQ = kHG * 128;             // 64 head rows x 128 B: one 64-dim chunk of Q
+constexpr int kChunkKV = kTileN * 128;         // 48 key rows x 128 B: one 64-dim chunk of a stage
+constexpr int kQBytes = 8 * kChunkQ;           // 64 heads x 512 dims
+constexpr int kStageBytes = 8 * kChunkKV;      // 48 keys x 512 dims
+constexpr int kPBytes = kHG * 128;             // 64 heads x 128-byte lines (48 keys bf16 used)
 constexpr int OFF_Q = 0;
 constexpr int OFF_KV = OFF_Q + kQBytes;
 constexpr int OFF_P = OFF_KV + kStages * kStageBytes;
 constexpr int OFF_RING = OFF_P + 2 * kPBytes;  // int32 pool rows of resolved slots
 constexpr int OFF_ML = OFF_RING + kRing * 4;   // float2 (m, l) per head
-constexpr int OFF_W = OFF_ML + kHG * 8;        // float per head: rescale / merge weights
-constexpr int OFF_MLX = OFF_W + kHG * 4;       // float2 [slice][head]: every slice's (m, l), pushed by the slices
-constexpr int OFF_MASK = OFF_MLX + kMaxCluster * kHG * 8;   // 64-bit key validity mask per stage
+constexpr int OFF_W = OFF_ML + kHG * 8;        // float per head: rescale factors
+constexpr int OFF_MASK = OFF_W + kHG * 4;      // 64-bit key validity mask per stage
 constexpr int OFF_BAR = OFF_MASK + kStages * 8;
 enum Bar {
     B_Q_FULL = 0,
@@ -101,17 +102,21 @@ enum Bar {
 constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;
 constexpr int OFF_MERGE = OFF_KV;              // [owned dim][64 heads] fp32, reuses the KV stages,
                                                // followed by the outgoing bf16 rows of the other dims;
-                                               // peers' bf16 blocks are staged in the Q area
+                                               // peers' bf16 blocks and every slice's (m, l) are
+                                               // staged in the Q area, the merge weights in the P area
 constexpr int kSmemUsed = OFF_MISC + 16;
-constexpr int kSmemAlloc = kSmemUsed + 1024;   // room to align the base to 1024 bytes
-static_assert(OFF_MERGE + kDim * kHG * 4 <= OFF_P, "merge buffer must fit in the KV stages");
-static_assert(kStages * kStageBytes >= kDim * kHG * 4, "owned fp32 rows + outgoing bf16 rows fit in the KV stages");
+constexpr int kSmemAlloc = kSmemUsed;          // the dynamic shared base is checked to be 1024-aligned
+// merge workspace per (token, grid split, head group): [Sc][512 dims][64 heads]
+// bf16 partial accumulators, then [Sc][64 heads] float2 (m, l)
+constexpr size_t kMergeRowsElems = (size_t)kDim * kHG;
+static_assert(kDim * kHG * 4 + 0 <= kStages * kStageBytes, "owned fp32 rows + outgoing bf16 rows fit in the KV stages");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
-static_assert(kRingHalf == kLoadThreads, "one slot per loader thread per chunk");
+static_assert(kRingHalf <= kLoadThreads, "one slot per loader thread per chunk");
 static_assert(kRingHalf % kTileN == 0 && kRingHalf / kTileN == 4, "four tiles per ring chunk");
-static_assert(6 * 80 * 128 <= kQBytes, "staged peer blocks (at most 6 x 80 dims, Sc = 7) must fit in the Q area");
-static_assert(7 * 64 * 128 <= kQBytes, "staged peer blocks (7 x 64 dims, Sc = 8) must fit in the Q area");
-static_assert(kMaxCluster * kHG * 4 <= kRing * 4, "merge weights must fit in the ring");
+static_assert(6 * 80 * 128 + 7 * 512 <= kQBytes, "staged peer blocks and (m, l) (Sc = 7) must fit in the Q area");
+static_assert(7 * 64 * 128 + 8 * 512 <= kQBytes, "staged peer blocks and (m, l) (Sc = 8) must fit in the Q area");
+static_assert(kMaxCluster * kHG * 4 <= 2 * kPBytes, "merge weights must fit in the P area");
+static_assert(kTileN % 16 == 0 && kTileN <= 64, "tile keys: whole K16 steps, one 64-bit mask");
 
 __device__ unsigned int g_dev_error;
 
@@ -291,14 +296,6 @@ __device__ __forceinline__ uint32_t sw128(uint32_t line, uint32_t piece) {
     return line * 128u + ((piece ^ (line & 7u)) << 4);
 }
 
-// Generic address of the same shared-memory object in CTA `rank` of the cluster.
-template <typename T>
-__device__ __forceinline__ const T* cluster_ptr(const T* local, uint32_t rank) {
-    uint64_t r;
-    asm volatile("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
-    return reinterpret_cast<const T*>(r);
-}
-
 // OR of `pred` over the `count` threads taking part in named barrier `id`.
 __device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred) {
     uint32_t r;
@@ -318,18 +315,22 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
 template <int KV_FORMAT>
 __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const uint32_t raw_base = smem_u32(smem_raw);
-    const uint32_t base = (raw_base + 1023u) & ~1023u;
-    uint8_t* smem = smem_raw + (base - raw_base);
+    const uint32_t base = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw;
+    if (base & 1023u) {
+        // the 128-byte swizzle atoms need a 1024-byte-aligned base (uniform
+        // over the grid, so every CTA of a cluster leaves here together)
+        if (threadIdx.x == 0) atomicOr(&g_dev_error, DSV4_DEV_ERR_PLAN);
+        return;
+    }
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const uint32_t rank = cluster_ctarank();
     const int G = p.groups;
-    const int grp = static_cast<int>(rank) % G;        // head group
-    const int cs = static_cast<int>(rank) / G;         // slice within the cluster
     const int Sc = p.csplits;
+    const int cs = static_cast<int>(cluster_ctarank());   // slice within the cluster
+    const int grp = blockIdx.x / Sc;                       // head group (one cluster per group)
     const int t = blockIdx.y;
     const int gsplit = blockIdx.z;
     const int split = gsplit * Sc + cs;
@@ -342,7 +343,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     int* ring = reinterpret_cast<int*>(smem + OFF_RING);
     float2* ml = reinterpret_cast<float2*>(smem + OFF_ML);
     float* wsm = reinterpret_cast<float*>(smem + OFF_W);
-    uint8_t* mask8 = smem + OFF_MASK;
     const uint32_t bars = base + OFF_BAR;
     auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
@@ -350,28 +350,18 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
 
     unsigned err = 0;
     if (tid == 0) DSV4_TR(0);
-    // the merge-weight threads (warps 0..3, lanes 0..15: head 16 * warp + lane)
-    // fetch their head's sink logit now, off the epilogue's critical path
-    float sink_l2 = -INFINITY;
-    if (warp < 4 && lane < 16 && 16 * warp + lane < hcount) sink_l2 = __ldg(p.sink + head0 + 16 * warp + lane) * kLog2e;
-
-    // ------------------------------------------------------------ set-up
-    // C4: each loader thread fetches the index of its first-chunk slot before
-    // the token's position is known, assuming the whole window is present
-    int idx_spec = -1;
-    if (is_loader && p.ratio == 4) {
-        const int e = split * p.chunk + lt - p.window;
-        if (e >= 0 && e < p.topk && lt < p.chunk) idx_spec = __ldg(p.topk_idx + (size_t)t * p.topk + e);
-    }
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream: barrier set-up and the TMEM allocation overlap its tail; every
+    // read of an input waits for its completion.
     if (tid == 0) {
         mbar_init(bar(B_Q_FULL), kSoftmaxWarps * 32);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(B_KV_FULL + s), kLoadThreads);
             mbar_init(bar(B_KV_EMPTY + s), 1);
-            mbar_init(bar(B_MASK_FULL + s), kLoadWarps);
+            mbar_init(bar(B_MASK_FULL + s), 1);
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(B_S_FULL + s), 1);
+            mbar_init(bar(B_S_FULL + s), 2);
             mbar_init(bar(B_S_FREE + s), kSoftmaxWarps * 32);
             mbar_init(bar(B_P_FULL + s), kSoftmaxWarps * 32);
             mbar_init(bar(B_P_FREE + s), 1);
@@ -381,6 +371,22 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         fence_mbar_init_cluster();
         *abort_flag = 0;
     }
+    if (warp == kQkWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // the merge-weight threads (warps 0..3, lanes 0..15: head 16 * warp + lane)
+    // fetch their head's sink logit now, off the epilogue's critical path
+    float sink_l2 = -INFINITY;
+    if (warp < 4 && lane < 16 && 16 * warp + lane < hcount) sink_l2 = __ldg(p.sink + head0 + 16 * warp + lane) * kLog2e;
+
+    // ------------------------------------------------------------ set-up
+    // C4: each loader thread fetches the index of its first-chunk slot before
+    // the token's position is known, assuming the whole window is present
+    int idx_spec = -1;
+    if (is_loader && p.ratio == 4 && lt < kRingHalf) {
+        const int e = split * p.chunk + lt - p.window;
+        if (e >= 0 && e < p.topk && lt < p.chunk) idx_spec = __ldg(p.topk_idx + (size_t)t * p.topk + e);
+    }
     // every thread derives the token's coordinates itself (same addresses; the
     // loads overlap the barrier set-up); thread 0 reports the errors
     TokenInfo ti;
@@ -389,7 +395,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         token_info(p, t, split, ti, e0);
         if (tid == 0) err |= e0;
     }
-    if (warp == kQkWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -411,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         const int nslots = ti.slot_end - ti.slot_begin;
         // chunk c of the slice (kRingHalf slots) goes to ring half c & 1
         auto resolve_chunk = [&](int c) {
+            if (lt >= kRingHalf) return;
             const int sl = ti.slot_begin + c * kRingHalf + lt;
             int row = -1;
             if (sl < ti.slot_end) {
@@ -424,28 +430,29 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             named_barrier_sync(1, kLoadThreads);
             if (lt == 0) DSV4_TR(3);
         }
+        constexpr int kR = kTileN / kLoadWarps;          // rows per loader warp
         for (int i = 0; i < ntiles; ++i) {
-            const int stage = i & 1;
+            const int stage = i % kStages, use = i / kStages;
             const int c = i >> 2;
             if ((i & 3) == 0 && i > 0) named_barrier_sync(1, kLoadThreads);   // chunk c resolved
             const int slot0 = ti.slot_begin + i * kTileN;
-            const int* rg = ring + (c & 1) * kRingHalf + (i & 3) * kTileN;   // this tile's 64 rows
+            const int* rg = ring + (c & 1) * kRingHalf + (i & 3) * kTileN;   // this tile's rows
+            const uint32_t dst_stage = sKV + stage * kStageBytes;
             if constexpr (KV_FORMAT == DSV4_KV_BF16) {
                 if (i >= kStages) {
-                    wait_bar(bar(B_KV_EMPTY + stage), ((i >> 1) - 1) & 1, abort_flag);
+                    wait_bar(bar(B_KV_EMPTY + stage), (use - 1) & 1, abort_flag);
                     fence_proxy_async();
                 }
-                const uint32_t dst_stage = sKV + stage * kStageBytes;
-#pragma unroll 4
-                for (int k = 0; k < kTileN / kLoadWarps; ++k) {
-                    const int r = lw * (kTileN / kLoadWarps) + k;
+#pragma unroll
+                for (int k = 0; k < kR; ++k) {
+                    const int r = lw * kR + k;
                     const int slot = slot0 + r;
                     const int row = slot < ti.slot_end ? rg[r] : -1;
                     const uint8_t* src = row >= 0 ? slot_row_ptr(p, ti, slot, row) : p.swa_rows;
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         const int piece = lane + 32 * h2;       // 16-byte piece of the 1 KB row
-                        const uint32_t dst = dst_stage + (piece >> 3) * kChunk + sw128(r, piece & 7);
+                        const uint32_t dst = dst_stage + (piece >> 3) * kChunkKV + sw128(r, piece & 7);
                         cp_async_16(dst, src + (row >= 0 ? piece * 16 : 0), row >= 0 ? 16u : 0u);
                     }
                 }
@@ -455,7 +462,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 // (e4m3 x the fp32 scale of their 64-dim block, rounded to bf16);
                 // lanes 28..31 copy 16 dims of the bf16 rope each.  The raw
                 // bytes are loaded before the stage is free.
-                constexpr int kR = kTileN / kLoadWarps;
                 uint4 raw[kR], raw2[kR];
                 float scl[kR];
 #pragma unroll
@@ -478,10 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                     }
                 }
                 if (i >= kStages) {
-                    wait_bar(bar(B_KV_EMPTY + stage), ((i >> 1) - 1) & 1, abort_flag);
+                    wait_bar(bar(B_KV_EMPTY + stage), (use - 1) & 1, abort_flag);
                     fence_proxy_async();
                 }
-                const uint32_t dst_stage = sKV + stage * kStageBytes;
 #pragma unroll
                 for (int k = 0; k < kR; ++k) {
                     const int r = lw * kR + k;
@@ -495,11 +500,11 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                             o[2 * e] = pack_bf16x2(f[0] * scl[k], f[1] * scl[k]);
                             o[2 * e + 1] = pack_bf16x2(f[2] * scl[k], f[3] * scl[k]);
                         }
-                        const uint32_t cbase = dst_stage + (lane >> 2) * kChunk;
+                        const uint32_t cbase = dst_stage + (lane >> 2) * kChunkKV;
                         st_shared_v4(cbase + sw128(r, 2 * (lane & 3)), o[0], o[1], o[2], o[3]);
                         st_shared_v4(cbase + sw128(r, 2 * (lane & 3) + 1), o[4], o[5], o[6], o[7]);
                     } else {
-                        const uint32_t cbase = dst_stage + 7 * kChunk;
+                        const uint32_t cbase = dst_stage + 7 * kChunkKV;
                         const int j = 2 * (lane - 28);
                         st_shared_v4(cbase + sw128(r, j), raw[k].x, raw[k].y, raw[k].z, raw[k].w);
                         st_shared_v4(cbase + sw128(r, j + 1), raw2[k].x, raw2[k].y, raw2[k].z, raw2[k].w);
@@ -508,15 +513,17 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 fence_proxy_async();
                 mbar_arrive(bar(B_KV_FULL + stage));
             }
-            {
-                // validity of the tile's 64 key slots, 8 per loader warp
-                constexpr int kRowsPerWarp = kTileN / kLoadWarps;
-                const int r = lw * kRowsPerWarp + (lane % kRowsPerWarp);
-                const bool valid = slot0 + r < ti.slot_end && rg[r] >= 0;
-                const unsigned bal = __ballot_sync(0xffffffffu, lane < kRowsPerWarp && valid);
-                if (lane == 0) mask8[stage * kLoadWarps + lw] = static_cast<uint8_t>(bal & 0xffu);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_MASK_FULL + stage));
+            if (lw == 0) {
+                // validity of the tile's key slots (lane l: rows l and 32 + l)
+                const bool v0 = slot0 + lane < ti.slot_end && rg[lane] >= 0;
+                const bool v1 = lane + 32 < kTileN && slot0 + lane + 32 < ti.slot_end && rg[lane + 32] >= 0;
+                const unsigned b0 = __ballot_sync(0xffffffffu, v0);
+                const unsigned b1 = __ballot_sync(0xffffffffu, v1);
+                if (lane == 0) {
+                    *reinterpret_cast<volatile uint64_t*>(smem + OFF_MASK + stage * 8) =
+                        static_cast<uint64_t>(b0) | (static_cast<uint64_t>(b1) << 32);
+                    mbar_arrive(bar(B_MASK_FULL + stage));
+                }
             }
             if (lt == 0 && i < 8) DSV4_TR(4 + i);
             // resolve the next chunk once this one's first two tiles are on their way
@@ -524,25 +531,31 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             if ((i & 3) == 1 && (c + 1) * kRingHalf < nslots) resolve_chunk(c + 1);
         }
         cp_async_wait_all();
-    } else if (warp == kQkWarp) {
-        // ============================================================ S = Q K^T issuer
+    } else if (warp == kQkWarp || warp == kQkWarp + 1) {
+        // ============================================================ S = Q K^T issuers
+        // warp kQkWarp + d accumulates dims 256 d .. 256 d + 255 into its own
+        // score half; softmax adds the halves
+        const int dh = warp - kQkWarp;
         if (lane == 0 && ntiles > 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kHG, kTileN, false, false);
             wait_bar(bar(B_Q_FULL), 0, abort_flag);
             fence_proxy_async();
             tc_fence_after();
             for (int i = 0; i < ntiles; ++i) {
-                wait_bar(bar(B_KV_FULL + (i & 1)), (i >> 1) & 1, abort_flag);
+                const int stage = i % kStages, use = i / kStages;
+                wait_bar(bar(B_KV_FULL + stage), use & 1, abort_flag);
                 if (i >= 2) wait_bar(bar(B_S_FREE + (i & 1)), ((i - 2) >> 1) & 1, abort_flag);
-                if (i < 8) DSV4_TR(12 + i);
+                if (dh == 0 && i < 8) DSV4_TR(12 + i);
                 fence_proxy_async();
                 tc_fence_after();
-                const uint32_t stg = sKV + (i & 1) * kStageBytes;
+                const uint32_t stg = sKV + stage * kStageBytes;
+                const uint32_t dcol = tmem + kTmemS + (i & 1) * (2 * kTileN) + dh * kTileN;
 #pragma unroll
-                for (int k = 0; k < kDim / 16; ++k) {
-                    const uint64_t a = smem_desc_sw128(sQ + (k >> 2) * kChunk + (k & 3) * 32, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(stg + (k >> 2) * kChunk + (k & 3) * 32, 16, 1024);
-                    mma_bf16_ss(tmem + kTmemS + (i & 1) * kTileN, a, b, idesc_qk, k > 0 ? 1u : 0u);
+                for (int kq = 0; kq < 16; ++kq) {
+                    const int k = 16 * dh + kq;
+                    const uint64_t a = smem_desc_sw128(sQ + (k >> 2) * kChunkQ + (k & 3) * 32, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(stg + (k >> 2) * kChunkKV + (k & 3) * 32, 16, 1024);
+                    mma_bf16_ss(dcol, a, b, idesc_qk, kq > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(B_S_FULL + (i & 1)));
             }
@@ -553,24 +566,25 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         if (lane == 0 && ntiles > 0) {
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kHG, true, false);
             for (int i = 0; i < ntiles; ++i) {
+                const int stage = i % kStages;
                 wait_bar(bar(B_P_FULL + (i & 1)), (i >> 1) & 1, abort_flag);
                 if (i < 8) DSV4_TR(20 + i);
                 tc_fence_after();
-                const uint32_t stg = sKV + (i & 1) * kStageBytes;
+                const uint32_t stg = sKV + stage * kStageBytes;
                 const uint32_t pbuf = sP + (i & 1) * kPBytes;
 #pragma unroll
                 for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
                     for (int kk = 0; kk < kTileN / 16; ++kk) {
                         // A = V^T (dims 128*mt.., keys 16*kk..): MN-major, 64-dim atoms one chunk apart
-                        const uint64_t a = smem_desc_sw128(stg + 2 * mt * kChunk + kk * 2048, kChunk, 1024);
+                        const uint64_t a = smem_desc_sw128(stg + 2 * mt * kChunkKV + kk * 2048, kChunkKV, 1024);
                         // B = P (heads x keys), K-major
                         const uint64_t b = smem_desc_sw128(pbuf + kk * 32, 16, 1024);
                         mma_bf16_ss(tmem + kTmemO + mt * kHG, a, b, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
                 mma_commit(bar(B_P_FREE + (i & 1)));
-                mma_commit(bar(B_KV_EMPTY + (i & 1)));
+                mma_commit(bar(B_KV_EMPTY + stage));
             }
             mma_commit(bar(B_O_FINAL));
         }
@@ -582,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             const uint8_t* qb = reinterpret_cast<const uint8_t*>(p.q) + ((size_t)t * p.H + head0) * 1024;
             for (int k = tid; k < kHG * 64; k += kSoftmaxWarps * 32) {
                 const int r = k >> 6, piece = k & 63;
-                const uint32_t dst = sQ + (piece >> 3) * kChunk + sw128(r, piece & 7);
+                const uint32_t dst = sQ + (piece >> 3) * kChunkQ + sw128(r, piece & 7);
                 const bool on = r < hcount && ntiles > 0;
                 cp_async_16(dst, on ? qb + (size_t)r * 1024 + piece * 16 : qb, on ? 16u : 0u);
             }
@@ -598,23 +612,25 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         const bool live = h < hcount;
         const bool owner = par == 0;                 // writes the head's per-head values
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(qd * 32) << 16);
+        constexpr int kJ = kTileN / 2;               // keys per thread
+        constexpr int kW = kJ / 2;                   // bf16 words each thread of the pair writes
         float m_run = -INFINITY, l_run = 0.f;
         for (int i = 0; i < ntiles; ++i) {
             const int sb = i & 1;
-            const int stage = i & 1;
-            float s[32];
+            const int stage = i % kStages, use = i / kStages;
+            float s[kJ];
             wait_bar(bar(B_S_FULL + sb), (i >> 1) & 1, abort_flag);
             if (tid == 0 && i < 8) DSV4_TR(28 + i);
             __syncwarp();
             tc_fence_after();
-            tmem_ld16x64b_x32(lane_addr + kTmemS + sb * kTileN, s);
+            tmem_ld16x64b_48_sum2(lane_addr + kTmemS + sb * (2 * kTileN), lane_addr + kTmemS + sb * (2 * kTileN) + kTileN, s);
             tc_fence_before();
             mbar_arrive(bar(B_S_FREE + sb));
-            wait_bar(bar(B_MASK_FULL + stage), (i >> 1) & 1, abort_flag);
+            wait_bar(bar(B_MASK_FULL + stage), use & 1, abort_flag);
             const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + OFF_MASK + stage * 8) >> par;
             float tmax = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < kJ; ++j) {
                 s[j] = ((mask >> (2 * j)) & 1ull) ? s[j] * p.scale_log2 : -INFINITY;
                 tmax = fmaxf(tmax, s[j]);
             }
@@ -625,11 +641,11 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 alpha = fast_exp2(m_run - tmax);
                 m_run = tmax;
             }
-            float pv[32];
+            float pv[kJ];
             float lsum = 0.f;
             const bool any = live && m_run != -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < kJ; ++j) {
                 // the denominator sums the fp32 probabilities; the bf16 copies
                 // only feed the PV product
                 pv[j] = any ? fast_exp2(s[j] - m_run) : 0.f;
@@ -637,23 +653,19 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             }
             l_run = l_run * alpha + lsum;
             // bf16 words (key 2w, key 2w + 1) of the head's line: the even-key
-            // thread builds words 0..15, the odd-key thread words 16..31
-            uint32_t wd[16];
-            {
-                uint32_t snd[8];
+            // thread builds words 0..kW-1, the odd-key thread words kW..2kW-1
+            uint32_t wd[kW];
 #pragma unroll
-                for (int m = 0; m < 8; ++m)
-                    snd[m] = par ? pack_bf16x2(pv[2 * m], pv[2 * m + 1]) : pack_bf16x2(pv[16 + 2 * m], pv[17 + 2 * m]);
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const uint32_t rcv = __shfl_xor_sync(0xffffffffu, snd[m], 2);
-                    const uint32_t own = par ? pack_bf16x2(pv[16 + 2 * m], pv[17 + 2 * m]) : pack_bf16x2(pv[2 * m], pv[2 * m + 1]);
-                    // own / rcv hold keys of j = 2m and 2m + 1 (offset 16 for the odd thread)
-                    const uint32_t ev = par ? rcv : own;   // even keys (j = 2m, 2m + 1 of the word range)
-                    const uint32_t od = par ? own : rcv;   // odd keys
-                    wd[2 * m] = __byte_perm(ev, od, 0x5410);      // (even j=2m, odd j=2m)
-                    wd[2 * m + 1] = __byte_perm(ev, od, 0x7632);  // (even j=2m+1, odd j=2m+1)
-                }
+            for (int m = 0; m < kW / 2; ++m) {
+                const uint32_t snd = par ? pack_bf16x2(pv[2 * m], pv[2 * m + 1])
+                                         : pack_bf16x2(pv[kW + 2 * m], pv[kW + 2 * m + 1]);
+                const uint32_t rcv = __shfl_xor_sync(0xffffffffu, snd, 2);
+                const uint32_t own = par ? pack_bf16x2(pv[kW + 2 * m], pv[kW + 2 * m + 1])
+                                         : pack_bf16x2(pv[2 * m], pv[2 * m + 1]);
+                const uint32_t ev = par ? rcv : own;   // even keys of words 2m, 2m + 1 of this thread's range
+                const uint32_t od = par ? own : rcv;   // odd keys
+                wd[2 * m] = __byte_perm(ev, od, 0x5410);
+                wd[2 * m + 1] = __byte_perm(ev, od, 0x7632);
             }
             if (i > 0) {
                 // a head whose running max moved scales its O^T column; each
@@ -678,26 +690,19 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             {
                 const uint32_t prow = sP + sb * kPBytes;
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    st_shared_v4(prow + sw128(h, 4 * par + q), wd[4 * q], wd[4 * q + 1], wd[4 * q + 2], wd[4 * q + 3]);
+                for (int q = 0; q < kW / 4; ++q)
+                    st_shared_v4(prow + sw128(h, (kW / 4) * par + q), wd[4 * q], wd[4 * q + 1], wd[4 * q + 2],
+                                 wd[4 * q + 3]);
             }
             fence_proxy_async();
             tc_fence_before();
             mbar_arrive(bar(B_P_FULL + sb));
             if (tid == 0 && i < 8) DSV4_TR(44 + i);
         }
-        // the head's denominator is the sum of its two halves; (m, l) goes to
-        // slot cs of every slice's table (its own included)
+        // the head's denominator is the sum of its two halves
         const float l_all = l_run + __shfl_xor_sync(0xffffffffu, l_run, 2);
-        if (owner) {
-            const float2 v = make_float2(live && ntiles > 0 ? m_run : -INFINITY, live && ntiles > 0 ? l_all : 0.f);
-            ml[h] = v;
-            const uint32_t dst = base + OFF_MLX + (cs * kHG + h) * 8;
-            for (int s2 = 0; s2 < Sc; ++s2) {
-                const uint32_t r = mapa(dst, static_cast<uint32_t>(s2 * G + grp));
-                asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(r), "f"(v.x), "f"(v.y) : "memory");
-            }
-        }
+        if (owner) ml[h] = make_float2(live && ntiles > 0 ? m_run : -INFINITY, live && ntiles > 0 ? l_all : 0.f);
+        fence_proxy_async();
     }
 
     // ------------------------------------------------------------ epilogue
@@ -705,30 +710,41 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     // dbase).  Every thread that reads O^T holds one value dim for all heads:
     // owned dims go to the fp32 rows T[dim][head]; the other dims go, as bf16
     // rows, to the outgoing area (row order = dim order without the owned
-    // range, so each peer's dims are one contiguous block), from where one
-    // bulk copy per peer stores them to the workspace.  After the cluster
-    // barrier each slice bulk-loads its dims from every peer (L2 and bulk
-    // copies move these far faster than distributed shared memory does).
-    // Bf16 rows are 128 B with 16-byte chunk q stored at q ^ (dim & 7).
+    // range, so each peer's dims are one contiguous block), from where each
+    // warp bulk-stores its rows to the workspace.  After the cluster barrier
+    // each slice bulk-loads its dims from every peer and every slice's (m, l)
+    // (L2 and bulk copies move these far faster than distributed shared
+    // memory does).  Bf16 rows are 128 B with 16-byte chunk q stored at
+    // q ^ (dim & 7).
     const int u_lo = (cs * 64) / Sc, u_hi = ((cs + 1) * 64) / Sc;
     const int nd = 8 * (u_hi - u_lo), dbase = 8 * u_lo;
     float* T = reinterpret_cast<float*>(smem + OFF_MERGE);
     const uint32_t sOut = base + OFF_MERGE + nd * kHG * 4;           // outgoing bf16 rows
-    uint16_t* mrg_t = p.merge + (((size_t)t * p.gsplits + gsplit) * G + grp) * Sc * (kDim * kHG);
+    uint16_t* mrg_t = p.merge + (((size_t)t * p.gsplits + gsplit) * G + grp) * Sc * (kMergeRowsElems + 4 * kHG);
+    float2* mrg_ml = reinterpret_cast<float2*>(mrg_t + Sc * kMergeRowsElems);
+    if (Sc > 1 && warp < kSoftmaxWarps) {
+        // this slice's (m, l) -> workspace slot cs (written by the four softmax warps)
+        named_barrier_sync(3, kSoftmaxWarps * 32);
+        if (tid == 0) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(mrg_ml + cs * kHG),
+                         "r"(base + OFF_ML), "r"(static_cast<uint32_t>(kHG * 8))
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+    }
     {
         // ============================================================ O^T read-out
-        // (quadrant qd, value tile mt) jobs: warp w takes (w % 4, w / 4); warps
-        // 2 and 3 also take mt = 3 of their quadrants.
+        // (quadrant qd, value tile mt) jobs: warp w takes (w % 4, w / 4); warp 3
+        // also takes (3, 3).
         if (ntiles > 0) {
             wait_bar(bar(B_O_FINAL), 0, abort_flag);
             if (tid == 0) DSV4_TR(52);
             tc_fence_after();
             fence_proxy_async();
-            if (tid == 0) DSV4_TR(53);
         }
         const int qd = warp & 3;
         __syncwarp();
-        const int njobs = (warp == 2 || warp == 3) ? 2 : 1;
+        const int njobs = warp == 3 ? 2 : 1;
         for (int jb = 0; jb < njobs; ++jb) {
             const int mt = jb == 0 ? warp >> 2 : 3;
             float o[64];
@@ -792,19 +808,20 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     if (tid == 0) DSV4_TR(60);
     const bool final_out = p.gsplits == 1;
     const uint32_t sIn = base + OFF_Q;                               // peers' bf16 rows [slot][dim]
-    float* W = reinterpret_cast<float*>(smem + OFF_RING);            // [slice][head] merge weights
-    const int issuer = kQkWarp * 32;
+    const float2* mlx = reinterpret_cast<const float2*>(smem + OFF_Q + (Sc - 1) * nd * 128);   // [slice][head]
+    float* W = reinterpret_cast<float*>(smem + OFF_P);               // [slice][head] merge weights
     if (Sc > 1) {
         tc_fence_before();
         cluster_sync();   // B: every slice's rows and (m, l) are published
         tc_fence_after();
         if (tid == 0) DSV4_TR(55);
-        if (tid == issuer) {
-            // this slice's dims from every other slice: one contiguous block each
+        if (tid == kQkWarp * 32) {
+            // this slice's dims from every other slice (one contiguous block
+            // each) and every slice's (m, l)
             asm volatile("fence.proxy.async.global;" ::: "memory");
             const uint32_t mb = bar(B_MERGE);
             asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb),
-                         "r"(static_cast<uint32_t>((Sc - 1) * nd * 128))
+                         "r"(static_cast<uint32_t>((Sc - 1) * nd * 128 + Sc * kHG * 8))
                          : "memory");
             int slot = 0;
             for (int s2 = 0; s2 < Sc; ++s2) {
@@ -817,17 +834,21 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                     : "memory");
                 ++slot;
             }
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    sIn + (Sc - 1) * nd * 128),
+                "l"(mrg_ml), "r"(static_cast<uint32_t>(Sc * kHG * 8)), "r"(mb)
+                : "memory");
         }
+        wait_bar(bar(B_MERGE), 0, abort_flag);
+    } else {
+        __syncthreads();   // T and (m, l) complete
     }
-    else {
-        __syncthreads();   // T complete
-    }
-    const float2* mlx = reinterpret_cast<const float2*>(smem + OFF_MLX);
+    if (tid == 0) DSV4_TR(59);
     if (warp < 4 && lane < 16) {
         // weights of every slice's accumulator for head h: exp(m_s - M) / L
         const int h = warp * 16 + lane;
         const bool live = h < hcount;
-        if (tid == 0) DSV4_TR(36);
         float2 mls[kMaxCluster];
 #pragma unroll
         for (int s2 = 0; s2 < kMaxCluster; ++s2)
@@ -835,7 +856,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         float M = -INFINITY;
 #pragma unroll
         for (int s2 = 0; s2 < kMaxCluster; ++s2) M = fmaxf(M, mls[s2].x);
-        if (tid == 0) DSV4_TR(37);
         const float sk = sink_l2;
         if (final_out) M = fmaxf(M, sk);
         float Lsum = 0.f;
@@ -850,7 +870,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
 #pragma unroll
         for (int s2 = 0; s2 < kMaxCluster; ++s2)
             if (s2 < Sc) W[s2 * kHG + h] = e[s2] * inv;
-        if (tid == 0) DSV4_TR(58);
         if (live && cs == 0) {
             if (final_out) {
                 if (p.lse) p.lse[(size_t)t * p.H + head0 + h] = (Lsum > 0.f ? M + log2f(Lsum) : -INFINITY) * kLn2;
@@ -860,8 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         }
     }
     __syncthreads();
-    if (Sc > 1) wait_bar(bar(B_MERGE), 0, abort_flag);
-    if (tid == 0) DSV4_TR(59);
+    if (tid == 0) DSV4_TR(58);
     // output: items (owned dim, 16-head quarter), consecutive threads on
     // consecutive dims so that every head's stores are contiguous
     for (int it = tid; it < nd * 4; it += kThreads) {
@@ -915,15 +933,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         }
     }
     if (tid == 0) DSV4_TR(61);
-    if (Sc > 1) {
-        // the workspace lines just copied are dead: drop them without write-back
-        for (int ln = tid; ln < (Sc - 1) * nd; ln += kThreads) {
-            int s2 = ln / nd;
-            if (s2 >= cs) ++s2;
-            const uint16_t* lp = mrg_t + ((size_t)s2 * kDim + dbase + ln % nd) * kHG;   // one 128-byte line
-            asm volatile("discard.global.L2 [%0], 128;" ::"l"(lp) : "memory");
-        }
-    }
     if (err) atomicOr(&g_dev_error, err);
     if (tid == 0) DSV4_TR(56);
     // no slice touches another's shared memory after barrier B
@@ -1034,14 +1043,14 @@ static int list_max(int ratio, int window, int topk, int max_seq_len) {
     return window + extra;
 }
 
-// Split plan: Sc key slices merged inside the kernel (one cluster of Sc x G
-// CTAs, G head groups) times Sg cluster groups merged by the combine kernel.
-// Cost in units of one 64-key tile: each wave of CTAs pays its slice's tiles
-// plus a fixed start-up and epilogue cost; the combine kernel and every extra
-// in-cluster slice add their merge work.
+// Split plan: Sc key slices merged inside the kernel (one cluster of Sc CTAs
+// per token and head group) times Sg cluster groups merged by the combine
+// kernel.  The cost is an estimate in microseconds from measured figures: a
+// 48-key tile per CTA, a fixed start-up and epilogue per wave of CTAs, the
+// in-cluster merge, and the combine kernel with its fp32 partials.
 static int make_plan(int T, int G, int lmax, int num_splits, const DeviceInfo& di, int& sc, int& sg) {
     const int tiles_total = (lmax + kTileN - 1) / kTileN;
-    const int max_sc = kMaxCluster / G;
+    const int max_sc = kMaxCluster;
     if (num_splits > 0) {
         sc = 1;
         for (int c = max_sc; c >= 1; --c)
@@ -1049,19 +1058,23 @@ static int make_plan(int T, int G, int lmax, int num_splits, const DeviceInfo& d
         sg = num_splits / sc;
         return DSV4_OK;
     }
+    constexpr double kTileUs = 1.3, kWaveUs = 4.0, kMergeUs = 1.5, kMergeSliceUs = 0.2;
+    constexpr double kCombineUs = 3.0, kCombineBytesPerUs = 5.0e6;
+    const int H = G * kHG;
     double best = 1e30;
     sc = 1;
     sg = 1;
     for (int c = 1; c <= max_sc; ++c) {
-        const int per_wave = di.max_clusters[c * G];
+        const int per_wave = di.max_clusters[c];
         for (int g = 1; g <= 64; ++g) {
             const int s = c * g;
             if (s > 1 && s > tiles_total) break;
-            const long long clusters = (long long)T * g;
+            const long long clusters = (long long)T * G * g;
             if (g > 1 && clusters > 4LL * per_wave) break;
             const long long waves = (clusters + per_wave - 1) / per_wave;
-            const double tiles = (double)lmax / s / kTileN;
-            const double cost = (double)waves * (tiles + 3.0) + (g > 1 ? 4.0 : 0.0) + 0.5 * (c - 1);
+            const double tiles = std::ceil((double)lmax / s / kTileN);
+            double cost = (double)waves * (tiles * kTileUs + kWaveUs + (c > 1 ? kMergeUs + kMergeSliceUs * (c - 1) : 0.0));
+            if (g > 1) cost += kCombineUs + (double)T * g * H * kDim * 4 / kCombineBytesPerUs;
             if (cost < best - 1e-9) { best = cost; sc = c; sg = g; }
         }
     }
@@ -1092,7 +1105,7 @@ static size_t ws_part_bytes(int T, int H, int sg) {
 }
 static size_t ws_merge_bytes(int T, int G, int sc, int sg) {
     if (sc <= 1) return 0;
-    return (size_t)T * sg * G * sc * kDim * kHG * sizeof(uint16_t);
+    return (size_t)T * sg * G * sc * (kMergeRowsElems * sizeof(uint16_t) + kHG * sizeof(float2));
 }
 static size_t workspace_bytes_for(int T, int H, int sc, int sg) {
     const int G = (H + kHG - 1) / kHG;
@@ -1201,17 +1214,21 @@ static int run(const Call& c) {
 
     cudaStream_t st = static_cast<cudaStream_t>(c.stream);
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3(sc * G, c.T, sg);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemAlloc;
     cfg.stream = st;
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = sc * G;
+    attr[0].val.clusterDim.x = sc;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch: the kernel waits for the previous
+    // kernel in the stream (griddepcontrol.wait) before it reads any input
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const cudaError_t le = c.swa->format == DSV4_KV_BF16
                                ? cudaLaunchKernelEx(&cfg, dsv4_attn_kernel<DSV4_KV_BF16>, p)
                                : cudaLaunchKernelEx(&cfg, dsv4_attn_kernel<DSV4_KV_FP8_PACKED>, p);

@@ -201,8 +201,10 @@ int dsv4_attn_c4_sparse_noalloc(const void* q, int32_t batch, int32_t num_heads,
 
 /* The split plan the library uses for these shapes on the current device
    (num_splits as passed to an entry point; 0 = automatic).  Writes the
-   number of key-list pieces merged on chip (1..4) and the number merged
-   through the workspace by the combine kernel.  Returns DSV4_OK or an error. */
+   number of key-list pieces merged inside the attention launch by one
+   thread-block cluster per token and 64-head group (1..8) and the number of
+   such cluster results merged through the workspace by the combine kernel.
+   Returns DSV4_OK or an error. */
 int dsv4_attn_plan(int32_t num_tokens, int32_t num_heads, int32_t compress_ratio,
                    int32_t window, int32_t topk, int32_t max_seq_len, int32_t num_splits,
                    int32_t* cluster_splits, int32_t* grid_splits);
