@@ -34,6 +34,23 @@ DEFAULT_WORKLOAD = "c4_decode"
 
 
 # ---------------------------------------------------------------- helpers
+def slowest_ms(ms, world, device):
+    """The job's time for a per-rank time `ms`: the maximum over the ranks of
+    the process group (every rank's replica has to finish)."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_tokens_per_s(tokens_per_rank_step, world, sec_per_step):
+    """Whole-job throughput: every rank processes its own batch each step."""
+    return world * tokens_per_rank_step / sec_per_step
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -312,14 +329,10 @@ def run_ours(args):
         dist.barrier()
     clocks.mark()
     clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = tt.item()
+    ms = slowest_ms(ev0.elapsed_time(ev1), world, dev)
     flags = attn.dsv4_attn_get_device_error(stream)
     sec_per_step = ms / 1e3 / args.steps
-    value = world * T / sec_per_step
+    value = job_tokens_per_s(T, world, sec_per_step)
 
     # ---- end to end through the public API with host buffers
     pin = lambda x: x.cpu().pin_memory()
@@ -356,12 +369,8 @@ def run_ours(args):
             e2e_step(k)
     e1.record(stream)
     torch.cuda.synchronize()
-    ems = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([ems], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ems = tt.item()
-    e2e_value = world * T / (ems / 1e3 / e2e_steps)
+    ems = slowest_ms(e0.elapsed_time(e1), world, dev)
+    e2e_value = job_tokens_per_s(T, world, ems / 1e3 / e2e_steps)
 
     # ---- oracle on the host, bounded sample of the same workload (rank 0, N=1)
     cpu_baseline = None
