@@ -382,10 +382,16 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     // ------------------------------------------------------------ set-up
     // C4: each loader thread fetches the index of its first-chunk slot before
     // the token's position is known, assuming the whole window is present
+    // (key list window + topk long; the slot layout is the one below)
     int idx_spec = -1;
     if (is_loader && p.ratio == 4 && lt < kRingHalf) {
-        const int e = split * p.chunk + lt - p.window;
-        if (e >= 0 && e < p.topk && lt < p.chunk) idx_spec = __ldg(p.topk_idx + (size_t)t * p.topk + e);
+        const int b0 = split * p.chunk, e0 = min(b0 + p.chunk, p.window + p.topk);
+        if (e0 > b0) {
+            const int nt = (e0 - b0 + kTileN - 1) / kTileN;
+            const int sl = b0 + lt - (nt * kTileN - (e0 - b0));
+            const int e = sl - p.window;
+            if (sl >= b0 && e >= 0 && e < p.topk) idx_spec = __ldg(p.topk_idx + (size_t)t * p.topk + e);
+        }
     }
     // every thread derives the token's coordinates itself (same addresses; the
     // loads overlap the barrier set-up); thread 0 reports the errors
@@ -414,12 +420,18 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             }
         }
         const int nslots = ti.slot_end - ti.slot_begin;
-        // chunk c of the slice (kRingHalf slots) goes to ring half c & 1
+        // Tile i holds the virtual slots 48 i .. 48 i + 47; virtual slot v is
+        // key slot slot_begin + v - shift, and v < shift are padding.  The short
+        // tile of a slice is its first one: it finishes early and frees a stage
+        // while the full tiles are still landing.
+        const int shift = ntiles * kTileN - nslots;
+        // chunk c of the slice (kRingHalf virtual slots) goes to ring half c & 1
         auto resolve_chunk = [&](int c) {
             if (lt >= kRingHalf) return;
-            const int sl = ti.slot_begin + c * kRingHalf + lt;
+            const int v = c * kRingHalf + lt;
+            const int sl = ti.slot_begin + v - shift;
             int row = -1;
-            if (sl < ti.slot_end) {
+            if (v >= shift && sl < ti.slot_end) {
                 const int idx = (p.ratio == 4 && sl >= ti.n_swa) ? c4_index(p, t, ti, sl, c == 0, idx_spec) : 0;
                 row = resolve_slot_idx(p, ti, sl, idx, err);
             }
@@ -435,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             const int stage = i % kStages, use = i / kStages;
             const int c = i >> 2;
             if ((i & 3) == 0 && i > 0) named_barrier_sync(1, kLoadThreads);   // chunk c resolved
-            const int slot0 = ti.slot_begin + i * kTileN;
+            const int slot0 = ti.slot_begin + i * kTileN - shift;           // key slot of row 0 (may be padding)
             const int* rg = ring + (c & 1) * kRingHalf + (i & 3) * kTileN;   // this tile's rows
             const uint32_t dst_stage = sKV + stage * kStageBytes;
             if constexpr (KV_FORMAT == DSV4_KV_BF16) {
@@ -447,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 for (int k = 0; k < kR; ++k) {
                     const int r = lw * kR + k;
                     const int slot = slot0 + r;
-                    const int row = slot < ti.slot_end ? rg[r] : -1;
+                    const int row = (slot >= ti.slot_begin && slot < ti.slot_end) ? rg[r] : -1;
                     const uint8_t* src = row >= 0 ? slot_row_ptr(p, ti, slot, row) : p.swa_rows;
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
@@ -468,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 for (int k = 0; k < kR; ++k) {
                     const int r = lw * kR + k;
                     const int slot = slot0 + r;
-                    const int row = slot < ti.slot_end ? rg[r] : -1;
+                    const int row = (slot >= ti.slot_begin && slot < ti.slot_end) ? rg[r] : -1;
                     raw[k] = raw2[k] = make_uint4(0, 0, 0, 0);
                     scl[k] = 0.f;
                     if (row >= 0) {
@@ -515,8 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             }
             if (lw == 0) {
                 // validity of the tile's key slots (lane l: rows l and 32 + l)
-                const bool v0 = slot0 + lane < ti.slot_end && rg[lane] >= 0;
-                const bool v1 = lane + 32 < kTileN && slot0 + lane + 32 < ti.slot_end && rg[lane + 32] >= 0;
+                const bool v0 = slot0 + lane >= ti.slot_begin && slot0 + lane < ti.slot_end && rg[lane] >= 0;
+                const bool v1 = lane + 32 < kTileN && slot0 + lane + 32 >= ti.slot_begin &&
+                                slot0 + lane + 32 < ti.slot_end && rg[lane + 32] >= 0;
                 const unsigned b0 = __ballot_sync(0xffffffffu, v0);
                 const unsigned b1 = __ballot_sync(0xffffffffu, v1);
                 if (lane == 0) {
