@@ -352,8 +352,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     if (tid == 0) DSV4_TR(0);
     // Launched as a programmatic dependent of the previous kernel in the
     // stream: barrier set-up and the TMEM allocation overlap its tail; every
-    // read of an input waits for its completion.
-    if (tid == 0) {
+    // read of an input waits for its completion.  The barriers are set up by
+    // the PV issuer warp, idle until the first probabilities, so that the
+    // threads whose loads start the gather are not delayed by it.
+    if (tid == kPvWarp * 32) {
         mbar_init(bar(B_Q_FULL), kSoftmaxWarps * 32);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(B_KV_FULL + s), kLoadThreads);
