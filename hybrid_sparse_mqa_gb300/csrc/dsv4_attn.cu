@@ -58,7 +58,10 @@ constexpr int kLoadThreads = kLoadWarps * 32;
 constexpr int kQkWarp = kSoftmaxWarps + kLoadWarps;   // S = Q K^T over dims 0..255 (owns the TMEM allocation);
                                                       // warp kQkWarp + 1 takes dims 256..511
 constexpr int kPvWarp = kQkWarp + 2;                  // issues O^T += V^T P^T
-constexpr int kThreads = (kPvWarp + 1) * 32;
+constexpr int kEpiWarp = kPvWarp + 1;                 // idle until the epilogue (one read-out job per warp)
+constexpr int kWarps = kEpiWarp + 1;
+constexpr int kThreads = kWarps * 32;
+static_assert(kWarps == 16, "one O^T read-out job (TMEM quadrant, value tile) per warp");
 constexpr int kMaxCluster = 8;
 constexpr float kRescaleLog2 = 8.0f; // lazy rescale threshold (factor 256)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -116,6 +119,7 @@ static_assert(kRingHalf % kTileN == 0 && kRingHalf / kTileN == 4, "four tiles pe
 static_assert(6 * 80 * 128 + 7 * 512 <= kQBytes, "staged peer blocks and (m, l) (Sc = 7) must fit in the Q area");
 static_assert(7 * 64 * 128 + 8 * 512 <= kQBytes, "staged peer blocks and (m, l) (Sc = 8) must fit in the Q area");
 static_assert(kMaxCluster * kHG * 4 <= 2 * kPBytes, "merge weights must fit in the P area");
+static_assert(kHG * 4 <= kRing * 4, "single-slice merge weights must fit in the ring");
 static_assert(kTileN % 16 == 0 && kTileN <= 64, "tile keys: whole K16 steps, one 64-bit mask");
 
 __device__ unsigned int g_dev_error;
@@ -604,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             mma_commit(bar(B_O_FINAL));
         }
         __syncwarp();
-    } else {
+    } else if (warp < kSoftmaxWarps) {
         // ============================================================ softmax
         // Q rows of this head group (1 KB each), zero past the last head
         {
@@ -722,110 +726,149 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
 
     // ------------------------------------------------------------ epilogue
     // Slice cs owns the 8-dim units [u_lo, u_hi) of the output (nd dims from
-    // dbase).  Every thread that reads O^T holds one value dim for all heads:
-    // owned dims go to the fp32 rows T[dim][head]; the other dims go, as bf16
-    // rows, to the outgoing area (row order = dim order without the owned
-    // range, so each peer's dims are one contiguous block), from where each
-    // warp bulk-stores its rows to the workspace.  After the cluster barrier
-    // each slice bulk-loads its dims from every peer and every slice's (m, l)
-    // (L2 and bulk copies move these far faster than distributed shared
-    // memory does).  Bf16 rows are 128 B with 16-byte chunk q stored at
-    // q ^ (dim & 7).
+    // dbase).  Warp w reads value dims 128 (w / 4) + 32 (w % 4) + lane of O^T
+    // (its TMEM lane quadrant) for all heads.  A thread whose dim is owned
+    // keeps its 64 values in registers; the other dims go, as bf16 rows, to
+    // the outgoing area (row order = dim order without the owned range, so
+    // each peer's dims are one contiguous block), from where each warp
+    // bulk-stores its rows to the workspace.  After the cluster barrier each
+    // slice bulk-loads its dims from every peer and every slice's (m, l) (L2
+    // and bulk copies move these far faster than distributed shared memory
+    // does), and the owners add them to their registers.  Bf16 rows are 128 B
+    // with 16-byte chunk q stored at q ^ (dim & 7).
     const int u_lo = (cs * 64) / Sc, u_hi = ((cs + 1) * 64) / Sc;
     const int nd = 8 * (u_hi - u_lo), dbase = 8 * u_lo;
-    float* T = reinterpret_cast<float*>(smem + OFF_MERGE);
-    const uint32_t sOut = base + OFF_MERGE + nd * kHG * 4;           // outgoing bf16 rows
+    const uint32_t sOut = base + OFF_MERGE;                          // outgoing bf16 rows
     uint16_t* mrg_t = p.merge + (((size_t)t * p.gsplits + gsplit) * G + grp) * Sc * (kMergeRowsElems + 4 * kHG);
     float2* mrg_ml = reinterpret_cast<float2*>(mrg_t + Sc * kMergeRowsElems);
-    if (Sc > 1 && warp < kSoftmaxWarps) {
-        // this slice's (m, l) -> workspace slot cs (written by the four softmax warps)
+    const bool final_out = p.gsplits == 1;
+    const uint32_t sIn = base + OFF_Q;                               // peers' bf16 rows [slot][dim]
+    const float2* mlx = reinterpret_cast<const float2*>(smem + OFF_Q + (Sc - 1) * nd * 128);   // [slice][head]
+    // [slice][head] merge weights: with Sc == 1 they are computed while the
+    // last PV may still read P, so they go to the ring (no longer read once the
+    // softmax has seen the last tile's mask); otherwise into P, after O_FINAL
+    float* W = reinterpret_cast<float*>(smem + (Sc == 1 ? OFF_RING : OFF_P));
+    // weights of every slice's accumulator for head h: exp(m_s - M) / L (the
+    // sink enters M and L once); thread (warp < 4, lane < 16) owns head 16 warp + lane
+    auto merge_weights = [&]() {
+        const int h = warp * 16 + lane;
+        const bool live = h < hcount;
+        float2 mls[kMaxCluster];
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxCluster; ++s2)
+            mls[s2] = s2 < Sc ? (s2 == cs ? ml[h] : mlx[s2 * kHG + h]) : make_float2(-INFINITY, 0.f);
+        float M = -INFINITY;
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxCluster; ++s2) M = fmaxf(M, mls[s2].x);
+        const float sk = sink_l2;
+        if (final_out) M = fmaxf(M, sk);
+        float Lsum = 0.f;
+        float e[kMaxCluster];
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxCluster; ++s2) {
+            e[s2] = (M != -INFINITY && mls[s2].x != -INFINITY) ? fast_exp2(mls[s2].x - M) : 0.f;
+            Lsum += mls[s2].y * e[s2];
+        }
+        if (final_out && M != -INFINITY && sk != -INFINITY) Lsum += fast_exp2(sk - M);
+        const float inv = (live && Lsum > 0.f) ? 1.f / Lsum : 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxCluster; ++s2)
+            if (s2 < Sc) W[s2 * kHG + h] = e[s2] * inv;
+        if (live && cs == 0) {
+            if (final_out) {
+                if (p.lse) p.lse[(size_t)t * p.H + head0 + h] = (Lsum > 0.f ? M + log2f(Lsum) : -INFINITY) * kLn2;
+            } else {
+                p.part_ml[((size_t)t * p.gsplits + gsplit) * p.H + head0 + h] = make_float2(M, Lsum);
+            }
+        }
+    };
+    // the bf16 output (or the fp32 partial of a grid split) of value dim d for
+    // all heads; consecutive lanes hold consecutive dims
+    auto write_dim = [&](int d, const float (&acc)[kHG]) {
+        if (final_out) {
+            __nv_bfloat16* o = p.out + ((size_t)t * p.H + head0) * kDim + d;
+#pragma unroll
+            for (int h = 0; h < kHG; ++h)
+                if (h < hcount) o[(size_t)h * kDim] = __float2bfloat16_rn(acc[h]);
+        } else {
+            float* o = p.part_o + (((size_t)t * p.gsplits + gsplit) * p.H + head0) * kDim + d;
+#pragma unroll
+            for (int h = 0; h < kHG; ++h)
+                if (h < hcount) o[(size_t)h * kDim] = acc[h];
+        }
+    };
+    if (warp < kSoftmaxWarps) {
+        // (m, l) of this slice are complete once the four softmax warps are
         named_barrier_sync(3, kSoftmaxWarps * 32);
-        if (tid == 0) {
+        if (Sc > 1 && tid == 0) {
             asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(mrg_ml + cs * kHG),
                          "r"(base + OFF_ML), "r"(static_cast<uint32_t>(kHG * 8))
                          : "memory");
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
+        if (Sc == 1 && lane < 16) merge_weights();
     }
-    {
-        // ============================================================ O^T read-out
-        // (quadrant qd, value tile mt) jobs: warp w takes (w % 4, w / 4); warp 3
-        // also takes (3, 3).
-        if (ntiles > 0) {
-            wait_bar(bar(B_O_FINAL), 0, abort_flag);
-            if (tid == 0) DSV4_TR(52);
-            tc_fence_after();
-            fence_proxy_async();
-        }
-        const int qd = warp & 3;
+    if (Sc == 1) __syncthreads();   // the weights are ready before the read-out
+    // ============================================================ O^T read-out
+    const int qd = warp & 3, mt = warp >> 2;
+    const int d = mt * 128 + qd * 32 + lane;                 // this thread's value dim
+    const bool owned = d >= dbase && d < dbase + nd;
+    float o[kHG];
+    if (ntiles > 0) {
+        wait_bar(bar(B_O_FINAL), 0, abort_flag);
+        if (tid == 0) DSV4_TR(52);
+        tc_fence_after();
+        fence_proxy_async();
         __syncwarp();
-        const int njobs = warp == 3 ? 2 : 1;
-        for (int jb = 0; jb < njobs; ++jb) {
-            const int mt = jb == 0 ? warp >> 2 : 3;
-            float o[64];
-            if (ntiles > 0) {
-                const uint32_t la = tmem + (static_cast<uint32_t>(qd * 32) << 16) + kTmemO + mt * kHG;
-                float a[32], b[32];
-                tmem_ld32(la, a);
-                tmem_ld32(la + 32, b);
+        const uint32_t la = tmem + (static_cast<uint32_t>(qd * 32) << 16) + kTmemO + mt * kHG;
+        float a[32], b[32];
+        tmem_ld32(la, a);
+        tmem_ld32(la + 32, b);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) { o[j] = a[j]; o[32 + j] = b[j]; }
-                if (tid == 0) DSV4_TR(54);
-            } else {
+        for (int j = 0; j < 32; ++j) { o[j] = a[j]; o[32 + j] = b[j]; }
+        if (tid == 0) DSV4_TR(54);
+    } else {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) o[j] = 0.f;
-            }
-            const int d = mt * 128 + qd * 32 + lane;           // this thread's value dim
-            if (d >= dbase && d < dbase + nd) {
-                const int dl = d - dbase;
-                float* row = T + dl * kHG;
+        for (int j = 0; j < kHG; ++j) o[j] = 0.f;
+    }
+    if (Sc == 1) {
+        // the slice is the whole key list: scale by the weight and write
 #pragma unroll
-                for (int q = 0; q < 16; ++q)   // 16-byte chunk q of the row, swizzled by dim
-                    *reinterpret_cast<float4*>(row + 4 * (q ^ (dl & 15))) =
-                        make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-            } else {
-                const int r = d < dbase ? d : d - nd;
-                const uint32_t row = sOut + r * 128;
+        for (int h = 0; h < kHG; ++h) o[h] *= W[h];
+        write_dim(d, o);
+    } else {
+        if (!owned) {
+            const int r = d < dbase ? d : d - nd;
+            const uint32_t row = sOut + r * 128;
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_shared_v4(row + ((q ^ (d & 7)) << 4), pack_bf16x2(o[8 * q], o[8 * q + 1]),
-                                 pack_bf16x2(o[8 * q + 2], o[8 * q + 3]), pack_bf16x2(o[8 * q + 4], o[8 * q + 5]),
-                                 pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
-            }
-            if (Sc > 1) {
-                // the warp's 32 dims: the rows outside the owned range go to the
-                // workspace rows [cs][dim][head] (at most two runs of rows)
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) {
-                    const int d0 = mt * 128 + qd * 32, d1 = d0 + 32;
-                    const int runs[2][2] = {{d0, min(d1, dbase)}, {max(d0, dbase + nd), d1}};
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const int a0 = runs[k][0], a1 = runs[k][1];
-                        if (a0 >= a1) continue;
-                        const int r0 = a0 < dbase ? a0 : a0 - nd;
-                        uint16_t* dst = mrg_t + ((size_t)cs * kDim + a0) * kHG;
-                        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                                     "r"(sOut + r0 * 128), "r"(static_cast<uint32_t>((a1 - a0) * 128))
-                                     : "memory");
-                    }
-                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                }
-            }
+            for (int q = 0; q < 8; ++q)
+                st_shared_v4(row + ((q ^ (d & 7)) << 4), pack_bf16x2(o[8 * q], o[8 * q + 1]),
+                             pack_bf16x2(o[8 * q + 2], o[8 * q + 3]), pack_bf16x2(o[8 * q + 4], o[8 * q + 5]),
+                             pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
         }
-        if (Sc > 1 && lane == 0) {
+        // the warp's 32 dims outside the owned range -> workspace rows [cs][dim][head]
+        // (at most two runs of rows)
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+            const int d0 = mt * 128 + qd * 32, d1 = d0 + 32;
+            const int runs[2][2] = {{d0, min(d1, dbase)}, {max(d0, dbase + nd), d1}};
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int a0 = runs[k][0], a1 = runs[k][1];
+                if (a0 >= a1) continue;
+                const int r0 = a0 < dbase ? a0 : a0 - nd;
+                uint16_t* dst = mrg_t + ((size_t)cs * kDim + a0) * kHG;
+                asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                             "r"(sOut + r0 * 128), "r"(static_cast<uint32_t>((a1 - a0) * 128))
+                             : "memory");
+            }
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
             asm volatile("fence.proxy.async.global;" ::: "memory");
         }
         __syncwarp();
-    }
-    if (tid == 0) DSV4_TR(60);
-    const bool final_out = p.gsplits == 1;
-    const uint32_t sIn = base + OFF_Q;                               // peers' bf16 rows [slot][dim]
-    const float2* mlx = reinterpret_cast<const float2*>(smem + OFF_Q + (Sc - 1) * nd * 128);   // [slice][head]
-    float* W = reinterpret_cast<float*>(smem + OFF_P);               // [slice][head] merge weights
-    if (Sc > 1) {
+        if (tid == 0) DSV4_TR(60);
         tc_fence_before();
         cluster_sync();   // B: every slice's rows and (m, l) are published
         tc_fence_after();
@@ -856,95 +899,45 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 : "memory");
         }
         wait_bar(bar(B_MERGE), 0, abort_flag);
-    } else {
-        __syncthreads();   // T and (m, l) complete
-    }
-    if (tid == 0) DSV4_TR(59);
-    if (warp < 4 && lane < 16) {
-        // weights of every slice's accumulator for head h: exp(m_s - M) / L
-        const int h = warp * 16 + lane;
-        const bool live = h < hcount;
-        float2 mls[kMaxCluster];
+        if (tid == 0) DSV4_TR(59);
+        if (warp < 4 && lane < 16) merge_weights();
+        __syncthreads();
+        if (tid == 0) DSV4_TR(58);
+        if (owned) {
+            // own accumulator x own weight + every peer's bf16 row x its weight
+            const int dl = d - dbase;
+            {
+                const float4* w4 = reinterpret_cast<const float4*>(W + cs * kHG);
 #pragma unroll
-        for (int s2 = 0; s2 < kMaxCluster; ++s2)
-            mls[s2] = s2 < Sc ? (Sc > 1 ? mlx[s2 * kHG + h] : ml[h]) : make_float2(-INFINITY, 0.f);
-        float M = -INFINITY;
-#pragma unroll
-        for (int s2 = 0; s2 < kMaxCluster; ++s2) M = fmaxf(M, mls[s2].x);
-        const float sk = sink_l2;
-        if (final_out) M = fmaxf(M, sk);
-        float Lsum = 0.f;
-        float e[kMaxCluster];
-#pragma unroll
-        for (int s2 = 0; s2 < kMaxCluster; ++s2) {
-            e[s2] = (M != -INFINITY && mls[s2].x != -INFINITY) ? fast_exp2(mls[s2].x - M) : 0.f;
-            Lsum += mls[s2].y * e[s2];
-        }
-        if (final_out && M != -INFINITY && sk != -INFINITY) Lsum += fast_exp2(sk - M);
-        const float inv = (live && Lsum > 0.f) ? 1.f / Lsum : 0.f;
-#pragma unroll
-        for (int s2 = 0; s2 < kMaxCluster; ++s2)
-            if (s2 < Sc) W[s2 * kHG + h] = e[s2] * inv;
-        if (live && cs == 0) {
-            if (final_out) {
-                if (p.lse) p.lse[(size_t)t * p.H + head0 + h] = (Lsum > 0.f ? M + log2f(Lsum) : -INFINITY) * kLn2;
-            } else {
-                p.part_ml[((size_t)t * p.gsplits + gsplit) * p.H + head0 + h] = make_float2(M, Lsum);
-            }
-        }
-    }
-    __syncthreads();
-    if (tid == 0) DSV4_TR(58);
-    // output: items (owned dim, 16-head quarter), consecutive threads on
-    // consecutive dims so that every head's stores are contiguous
-    for (int it = tid; it < nd * 4; it += kThreads) {
-        const int dl = it % nd, hq = it / nd;
-        const int d = dbase + dl;
-        float acc[16];
-        {
-            const float* row = T + dl * kHG;
-            const float4* wown = reinterpret_cast<const float4*>(W + cs * kHG + 16 * hq);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 v = *reinterpret_cast<const float4*>(row + 4 * ((4 * hq + q) ^ (dl & 15)));
-                const float4 w = wown[q];
-                acc[4 * q] = w.x * v.x;
-                acc[4 * q + 1] = w.y * v.y;
-                acc[4 * q + 2] = w.z * v.z;
-                acc[4 * q + 3] = w.w * v.w;
-            }
-        }
-        int slot = 0;
-        for (int s2 = 0; s2 < Sc; ++s2) {
-            if (s2 == cs) continue;
-            const float4* ws = reinterpret_cast<const float4*>(W + s2 * kHG + 16 * hq);
-            const uint32_t row = sIn + (slot * nd + dl) * 128;
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const float4 v = ld_shared_v4(row + (((2 * hq + q) ^ (d & 7)) << 4));
-                const uint32_t w4[4] = {__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
-                                        __float_as_uint(v.w)};
-                const float4 wa = ws[2 * q], wb = ws[2 * q + 1];
-                const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    acc[8 * q + 2 * e] += wv[2 * e] * __uint_as_float(w4[e] << 16);
-                    acc[8 * q + 2 * e + 1] += wv[2 * e + 1] * __uint_as_float(w4[e] & 0xffff0000u);
+                for (int q = 0; q < kHG / 4; ++q) {
+                    const float4 w = w4[q];
+                    o[4 * q] *= w.x;
+                    o[4 * q + 1] *= w.y;
+                    o[4 * q + 2] *= w.z;
+                    o[4 * q + 3] *= w.w;
                 }
             }
-            ++slot;
-        }
-        const int h0 = 16 * hq;
-        if (final_out) {
-            __nv_bfloat16* o = p.out + ((size_t)t * p.H + head0 + h0) * kDim + d;
+            int slot = 0;
+            for (int s2 = 0; s2 < Sc; ++s2) {
+                if (s2 == cs) continue;
+                const float4* ws = reinterpret_cast<const float4*>(W + s2 * kHG);
+                const uint32_t row = sIn + (slot * nd + dl) * 128;
 #pragma unroll
-            for (int h = 0; h < 16; ++h)
-                if (h0 + h < hcount) o[(size_t)h * kDim] = __float2bfloat16_rn(acc[h]);
-        } else {
-            float* o = p.part_o + (((size_t)t * p.gsplits + gsplit) * p.H + head0 + h0) * kDim + d;
+                for (int q = 0; q < 8; ++q) {
+                    const float4 v = ld_shared_v4(row + ((q ^ (d & 7)) << 4));
+                    const uint32_t w4[4] = {__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                                            __float_as_uint(v.w)};
+                    const float4 wa = ws[2 * q], wb = ws[2 * q + 1];
+                    const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-            for (int h = 0; h < 16; ++h)
-                if (h0 + h < hcount) o[(size_t)h * kDim] = acc[h];
+                    for (int e = 0; e < 4; ++e) {
+                        o[8 * q + 2 * e] += wv[2 * e] * __uint_as_float(w4[e] << 16);
+                        o[8 * q + 2 * e + 1] += wv[2 * e + 1] * __uint_as_float(w4[e] & 0xffff0000u);
+                    }
+                }
+                ++slot;
+            }
+            write_dim(d, o);
         }
     }
     if (tid == 0) DSV4_TR(61);
