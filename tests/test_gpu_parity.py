@@ -163,3 +163,29 @@ def test_fp8_h128(attn):
 def test_full_size_c4_verify_fp8_sampled(attn):
     inp = synth.make_inputs("c4_verify_fp8", device="cuda")
     run_and_compare(attn, inp, tokens=[0, 3, 130, 255])
+
+
+def test_back_to_back_calls_read_inputs_after_the_previous_kernel(attn):
+    """Attention launches carry programmatic stream serialisation: a launch may
+    start while the previous kernel of the stream drains, but must read none
+    of its inputs before that kernel has finished.  Chain calls on one stream
+    without synchronising, each taking the previous call's output as its
+    query (including a grid-split plan, whose combine kernel precedes the next
+    launch), and compare every link with the oracle on the query it got."""
+    import dataclasses
+    inp = small("c4", 64, (3000, 9000, 20000, 65000, 700, 40000), seed=91)
+    links = []
+    q = inp.q
+    for k, splits in enumerate((0, 16, 0, 4, 0)):
+        g = dataclasses.replace(inp, q=q)
+        out, lse = attn.run_inputs(g, num_splits=splits)
+        links.append((g, out, lse))
+        q = out
+    torch.cuda.synchronize()
+    assert attn.dsv4_attn_get_device_error() == 0
+    for k, (g, out, lse) in enumerate(links):
+        res = O.dsv4_attention(**g.oracle_kwargs())
+        err = np.abs(out.float().cpu().numpy() - res.out)
+        assert err.max() <= TOL_MAX_BF16, (k, float(err.max()))
+        assert err.mean() <= TOL_MEAN_BF16, (k, float(err.mean()))
+        assert np.abs(lse.cpu().numpy() - res.lse).max() <= TOL_LSE, k
