@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -69,10 +70,15 @@ def measured_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the kernel sources' code: comments and whitespace do not count,
+    so a stored ncu figure stays valid until the code itself changes."""
     h = hashlib.sha256()
     for rel in ("hybrid_sparse_mqa_gb300/csrc/dsv4_attn.cu", "hybrid_sparse_mqa_gb300/csrc/dsv4_device.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

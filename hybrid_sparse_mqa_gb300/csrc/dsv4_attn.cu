@@ -10,20 +10,20 @@
 //   (through L2); Sg groups of clusters merge through the workspace and the
 //   combine kernel.  With H = 128 the two head groups of a slice read the
 //   same rows.
-// * Per 64-key tile: eight loader warps resolve key slots to pool rows (SWA
-//   page table, C4 index list, C128 range) one 256-slot chunk ahead of use and
+// * Per 48-key tile: eight loader warps resolve key slots to pool rows (SWA
+//   page table, C4 index list, C128 range) one 192-slot chunk ahead of use and
 //   gather the 1 KB rows with 16-byte cp.async into a 128-byte-swizzled shared
-//   tile.  One MMA warp computes S = Q K^T on tcgen05 (M = 64 heads, N = 64
-//   keys, K = 512; fp32 in TMEM).  Four softmax warps read S with the 16-lane
-//   TMEM access shape: the two threads t and t ^ 2 hold the even and odd key
-//   columns of one head, so the online softmax (lazily updated running max,
-//   fp32 denominator) needs one shuffle per reduction; the bf16
-//   probabilities go into the head's 128-byte line.  A second MMA warp
-//   accumulates O^T += V^T P^T (M = 128 of the 512 value dims per MMA, N = 64
-//   heads, K = 64 keys) into 4 x 64 TMEM columns; V is the same shared tile
-//   read MN-major (K and V are the same row).  Each tcgen05.mma costs its
-//   issuing thread about as long as a small MMA takes to run, so the two
-//   products are issued from two warps and overlap.
+//   tile.  Two MMA warps compute S = Q K^T on tcgen05, each over one half of
+//   the 512 dims into its own fp32 TMEM accumulator (M = 64 heads, N = 48
+//   keys).  Four softmax warps read S with the 16-lane TMEM access shape: the
+//   two threads t and t ^ 2 hold the even and odd key columns of one head, so
+//   the online softmax (lazily updated running max, fp32 denominator) needs
+//   one shuffle per reduction; the bf16 probabilities go into the head's
+//   128-byte line.  A third MMA warp accumulates O^T += V^T P^T (M = 128 of
+//   the 512 value dims per MMA, N = 64 heads, K = 48 keys) into 4 x 64 TMEM
+//   columns; V is the same shared tile read MN-major (K and V are the same
+//   row).  Each tcgen05.mma costs its issuing thread about as long as a small
+//   MMA takes to run, so the products are issued from three warps and overlap.
 // * At the end the sink adds exp(sink - M) to each head's denominator, the
 //   slices are merged with log-sum-exp weights and the bf16 output written.
 //
