@@ -6,10 +6,11 @@ sequence lengths, query boundaries and top-k index lists.  It holds none of
 the step's arithmetic, so both the CUDA path and the float64 oracle can take
 their inputs from it.
 
-The FP8 packer below produces the packed KV rows that the cache writer would
-store (448 e4m3 nope values, 64 bf16 rope values, 7 fp32 scales, 608-byte
-stride); that writer is outside the attention step, so for the step these rows
-are generated inputs.
+Packed FP8 pools are drawn directly in their stored layout (448 e4m3 nope
+codes, 64 bf16 rope values, 7 fp32 block scales, 608-byte stride): random
+finite e4m3 codes, random positive scales and random bf16 rope values.  No
+quantisation happens here; the cache writer that quantises bf16 rows is part
+of the library (dsv4_kv_store), and its tests feed it bf16 rows drawn below.
 
 Shapes follow the five workloads of the step:
   swa_tiny       batch 2, seq_lens (7,7), H=8, SWA only
@@ -135,24 +136,6 @@ class Inputs:
 
 
 # --------------------------------------------------------------------------
-def pack_fp8_rows(rows_bf16: torch.Tensor) -> torch.Tensor:
-    """bf16 [n, 512] -> packed uint8 [n, 608]: per 64-value nope block,
-    scale = amax / 448 (1 when the block is all zero), codes = round-to-nearest
-    e4m3 of value / scale; rope kept as bf16; scales stored as fp32."""
-    n = rows_bf16.shape[0]
-    x = rows_bf16.float()
-    nope = x[:, :NOPE].reshape(n, NOPE // BLOCK, BLOCK)
-    amax = nope.abs().amax(dim=2)
-    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
-    codes = (nope / scale[:, :, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
-    out = torch.zeros(n, FP8_STRIDE, dtype=torch.uint8, device=rows_bf16.device)
-    out[:, :NOPE] = codes.reshape(n, NOPE).view(torch.uint8)
-    out[:, NOPE:NOPE + 2 * ROPE] = rows_bf16[:, NOPE:].contiguous().view(torch.uint8).reshape(n, 2 * ROPE)
-    out[:, NOPE + 2 * ROPE:NOPE + 2 * ROPE + 4 * (NOPE // BLOCK)] = \
-        scale.contiguous().view(torch.uint8).reshape(n, 4 * (NOPE // BLOCK))
-    return out
-
-
 def _randn_bf16(shape, gen, device, chunk_rows=1 << 20):
     """N(0,1)*0.5 in bf16, drawn in chunks to bound temporary fp32 memory."""
     out = torch.empty(shape, dtype=torch.bfloat16, device=device)
@@ -170,7 +153,21 @@ def _pool(num_rows, kv_format, gen, device):
     step = 1 << 18
     for r0 in range(0, num_rows, step):
         r1 = min(num_rows, r0 + step)
-        out[r0:r1] = pack_fp8_rows(_randn_bf16((r1 - r0, DIM), gen, device))
+        out[r0:r1] = _fp8_rows(r1 - r0, gen, device)
+    return out
+
+
+def _fp8_rows(n, gen, device):
+    """n packed FP8 rows: finite e4m3 codes uniform over the 254 non-NaN codes
+    (0x7F and 0xFF are skipped), block scales uniform in [0.005, 0.012),
+    bf16 rope ~ N(0,1)*0.5, zero padding."""
+    out = torch.zeros(n, FP8_STRIDE, dtype=torch.uint8, device=device)
+    r = torch.randint(0, 254, (n, NOPE), generator=gen, device=device, dtype=torch.int32)
+    out[:, :NOPE] = (r + (r >= 0x7F).to(torch.int32)).to(torch.uint8)
+    out[:, NOPE:NOPE + 2 * ROPE] = _randn_bf16((n, ROPE), gen, device).view(torch.uint8).reshape(n, 2 * ROPE)
+    scales = 0.005 + 0.007 * torch.rand((n, NOPE // BLOCK), generator=gen, device=device)
+    out[:, NOPE + 2 * ROPE:NOPE + 2 * ROPE + 4 * (NOPE // BLOCK)] = \
+        scales.float().contiguous().view(torch.uint8).reshape(n, 4 * (NOPE // BLOCK))
     return out
 
 

@@ -36,6 +36,16 @@ Sources (page title, section):
     pairs a 128-token sliding window with C4 (4:1 compression, top-512 sparse)
     or C128 (128:1 compression, dense).
 
+The oracle also states the cache write that precedes the step: a new key row
+(512 bf16 values after RoPE) is stored at its request's slot of a paged pool,
+packed to FP8 when the pool holds packed rows ("DeepSeek-V4 Attention: Query,
+Cache Write and History Addressing", section 3: the current token's
+representation is written into its SWA slot before the attention backend
+reads the cache; "SGLang DeepSeek-V4 Attention Test Capability Matrix",
+"Input And Config Coverage" and "Reference Implementation Notes": the
+production pack-and-store path writes packed FP8 nope + BF16 rope rows, 584
+bytes per token, into the SWA and extra pools).
+
 Readings where the pages are silent (each is also listed in the design notes):
   R1 the current token is inside its own window: keys are positions
      max(0, p - window + 1) .. p;
@@ -51,6 +61,16 @@ Readings where the pages are silent (each is also listed in the design notes):
      scale per 64 nope values, stride 608 bytes;
   R8 e4m3 is the OCP FP8 E4M3 format (bias 7, subnormals, no infinities,
      S.1111.111 is NaN).
+  R13 the packer's scale of a 64-value nope block is amax / 448 in float32
+     (1 when the block is all zero) and each code is the e4m3 value nearest
+     to value / scale in float32 (ties to even; beyond 448 it saturates); the
+     quantisation decision is taken in float32, the precision the writer
+     computes in;
+  R14 a new row goes to pool row page_table[r][i // 256] * 256 + i % 256 of
+     its request row r, where i is its logical row number (the token position
+     for the SWA pool, the compressed-row number for an extra pool); a row
+     whose request row, logical page or physical page is outside the tables
+     or the pool is not written and is reported.
 
 Parity pins: every function here is pinned by the CPU tests against something
 other than itself (closed forms, brute force, textbook softmax, library e4m3
@@ -77,6 +97,7 @@ ERR_SWA_PAGE = 1
 ERR_EXTRA_PAGE = 2
 ERR_INDEX_RANGE = 4
 ERR_TOKEN_POSITION = 8
+ERR_STORE_ROW = 128
 
 
 # --------------------------------------------------------------------------
@@ -234,6 +255,90 @@ def unpack_fp8_rows(raw):
     rope_bits = np.ascontiguousarray(raw[:, NOPE_DIM:NOPE_DIM + 2 * ROPE_DIM]).view('<u2')
     rope = bf16_bits_to_f64(rope_bits)
     return np.concatenate([nope, rope], axis=1)
+
+
+def e4m3_from_f32(x):
+    """float32 values -> OCP FP8 E4M3 codes (uint8), rounding to nearest with
+    ties to even and saturating to +-448 (readings R8, R13).
+
+    A magnitude a >= 2^-6 is normal: a = (1 + m/8) * 2^e with the 3-bit
+    mantissa m = round((a / 2^e - 1) * 8); a carry (m = 8) moves to the next
+    binade.  Below 2^-6 the step is 2^-9 and the code is round(a / 2^-9)
+    (a result of 8 is the smallest normal, code 8).  Values past 448 after
+    rounding become 448.  The sign is the sign bit of the input (so -0.0 and
+    negative values that round to zero give 0x80).  NaN gives 0x7F.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    a = np.abs(x).astype(np.float64)
+    sign = np.where(np.signbit(x), 0x80, 0x00).astype(np.int64)
+    fin = np.where(np.isfinite(a), a, 1.0)
+    _, ex = np.frexp(fin)                        # fin = f * 2^ex, f in [0.5, 1)
+    e = ex.astype(np.int64) - 1                  # fin in [2^e, 2^(e+1))
+    m = np.rint((fin / np.exp2(e.astype(np.float64)) - 1.0) * 8.0).astype(np.int64)
+    carry = m == 8
+    e = np.where(carry, e + 1, e)
+    m = np.where(carry, 0, m)
+    normal_code = ((e + 7) << 3) | m
+    sub_code = np.rint(np.minimum(fin, 1.0) / 2.0 ** -9).astype(np.int64)   # 0 .. 8 below 2^-6
+    code = np.where(a >= 2.0 ** -6, normal_code, sub_code)
+    code = np.where((a >= 2.0 ** -6) & ((e > 8) | ((e == 8) & (m == 7))), 0x7E, code)
+    code = np.where(np.isinf(a), 0x7E, code)
+    code = code | sign
+    code = np.where(np.isnan(a), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def pack_fp8_rows(bits):
+    """bf16 rows (uint16 bit patterns [n, 512]) -> packed FP8 rows (uint8
+    [n, 608]) in the layout of reading R7, quantised as reading R13.
+
+    Per 64-value nope block b: amax = max |x|, scale = amax / 448 in float32
+    (1.0 for an all-zero block), code = e4m3(x / scale) in float32.  The 64
+    rope values keep their bf16 bits; the 7 scales are stored as float32;
+    bytes 604..607 are zero.
+    """
+    bits = np.ascontiguousarray(np.asarray(bits, dtype=np.uint16))
+    n = bits.shape[0]
+    x = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)        # exact
+    nope = x[:, :NOPE_DIM].reshape(n, NOPE_DIM // FP8_BLOCK, FP8_BLOCK)
+    amax = np.max(np.abs(nope), axis=2)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    codes = e4m3_from_f32((nope / scale[:, :, None]).astype(np.float32))
+    out = np.zeros((n, FP8_ROW_BYTES), dtype=np.uint8)
+    out[:, :NOPE_DIM] = codes.reshape(n, NOPE_DIM)
+    out[:, NOPE_DIM:NOPE_DIM + 2 * ROPE_DIM] = bits[:, NOPE_DIM:].astype("<u2").view(np.uint8)
+    out[:, NOPE_DIM + 2 * ROPE_DIM:NOPE_DIM + 2 * ROPE_DIM + 4 * (NOPE_DIM // FP8_BLOCK)] = \
+        scale.astype("<f4").view(np.uint8).reshape(n, 4 * (NOPE_DIM // FP8_BLOCK))
+    return out
+
+
+def kv_store(pool, bits, req_rows, positions, page_table, kv_format):
+    """Write new key rows into a paged pool (readings R7, R13, R14).
+
+    pool: uint16 [rows, 512] (bf16) or uint8 [rows, 608] (packed FP8);
+    bits: uint16 [n, 512] bf16 bit patterns of the new rows; req_rows[i] is
+    the page-table row of row i's request and positions[i] its logical row
+    number.  Returns (new pool, OR of ERR_* bits); rows that cannot be placed
+    are skipped and reported as ERR_STORE_ROW.
+    """
+    out = np.array(pool, copy=True)
+    bits = np.asarray(bits, dtype=np.uint16)
+    if kv_format == "fp8":
+        packed = pack_fp8_rows(bits)
+    elif kv_format != "bf16":
+        raise ValueError(f"unknown kv format {kv_format}")
+    num_pages = out.shape[0] // PAGE_SIZE
+    errors = 0
+    for i in range(bits.shape[0]):
+        r = int(req_rows[i])
+        dest = -1
+        if 0 <= r < page_table.shape[0]:
+            dest = physical_row(page_table, r, int(positions[i]), num_pages)
+        if dest < 0:
+            errors |= ERR_STORE_ROW
+            continue
+        out[dest] = packed[i] if kv_format == "fp8" else bits[i]
+    return out, errors
 
 
 def pool_rows_f64(pool, rows, kv_format):

@@ -185,7 +185,7 @@ def pin_fp8_unpack_closed_form():
 def pin_fp8_unpack_roundtrip():
     g = torch.Generator().manual_seed(3)
     x = (torch.randn(64, 512, generator=g) * 0.5).to(torch.bfloat16)
-    raw = synth.pack_fp8_rows(x).numpy()
+    raw = O.pack_fp8_rows(x.view(torch.int16).numpy().view(np.uint16))
     got = O.unpack_fp8_rows(raw)
     xf = x.double().numpy()
     scales = raw[:, 576:604].copy().view("<f4").astype(np.float64)
@@ -196,6 +196,146 @@ def pin_fp8_unpack_roundtrip():
     assert np.all(err <= np.abs(xf[:, :448]) * 2.0 ** -4 + step * 2.0 ** -10 + 1e-300)
     assert np.array_equal(got[:, 448:], xf[:, 448:])
     assert np.array_equal(got, _torch_fp8_rows_to_f64(raw))
+
+
+def _torch_e4m3(x):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
+
+
+def _torch_pack_fp8(bits):
+    """The packer of reading R13 written with torch's float32 arithmetic and
+    its float8_e4m3fn cast (which rounds to nearest even; no value here
+    reaches its NaN range at 464 and above)."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    n = bits.shape[0]
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float()
+    nope = x[:, :448].reshape(n, 7, 64)
+    amax = nope.abs().amax(dim=2)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    out = np.zeros((n, 608), dtype=np.uint8)
+    out[:, :448] = (nope / scale[:, :, None]).to(torch.float8_e4m3fn).view(torch.uint8).reshape(n, 448).numpy()
+    out[:, 448:576] = bits[:, 448:].view(np.uint8).reshape(n, 128)
+    out[:, 576:604] = scale.numpy().astype("<f4").view(np.uint8).reshape(n, 28)
+    return out
+
+
+def _bf16_bits(x):
+    """float32 values that are exact in bf16 -> their bf16 bit patterns."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert np.all((x.view(np.uint32) & 0xFFFF) == 0)
+    return (x.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def pin_e4m3_encode_library():
+    # every finite bf16 value below the saturation edge, random float32 values
+    # over the whole range, and the exact midpoints between neighbouring e4m3
+    # values (ties go to the even code), against torch's float8_e4m3fn cast
+    b = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    f = (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    parts = [f[np.isfinite(f)]]
+    rng = np.random.default_rng(7)
+    parts.append((rng.standard_normal(20000) * np.exp2(rng.uniform(-14, 9, 20000))).astype(np.float32))
+    dec = O.e4m3_to_f64(np.arange(0, 0x7F, dtype=np.uint8))          # 0 .. 448, increasing
+    mids = (dec[:-1] + dec[1:]) / 2
+    assert np.array_equal(mids.astype(np.float32).astype(np.float64), mids)   # exact in float32
+    parts += [mids.astype(np.float32), -mids.astype(np.float32)]
+    x = np.concatenate(parts)
+    x = x[np.abs(x) < 464]
+    assert np.array_equal(O.e4m3_from_f32(x), _torch_e4m3(x))
+
+
+def pin_e4m3_encode_closed_form():
+    codes = np.arange(256, dtype=np.uint8)
+    finite = (codes & 0x7F) != 0x7F
+    vals = O.e4m3_to_f64(codes[finite]).astype(np.float32)
+    assert np.array_equal(O.e4m3_from_f32(vals), codes[finite])       # each finite code encodes its value
+    sat = np.array([464.0, 470.0, 1.0e6, np.inf, -500.0, -np.inf], dtype=np.float32)
+    assert O.e4m3_from_f32(sat).tolist() == [0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+    assert O.e4m3_from_f32(np.array([np.nan], dtype=np.float32)).tolist() == [0x7F]
+    # half the smallest subnormal rounds to (signed) zero, 1.5 of it to 2 steps
+    tiny = np.array([2.0 ** -10, -2.0 ** -10, 1.5 * 2.0 ** -9], dtype=np.float32)
+    assert O.e4m3_from_f32(tiny).tolist() == [0x00, 0x80, 0x02]
+
+
+def pin_fp8_pack_closed_form():
+    # block b < 6 holds 448 * 2^-b and -224 * 2^-b: scale 2^-b exactly, codes
+    # 0x7E (448) and 0xF6 (-224); block 6 is all zero: scale 1, codes 0; the
+    # rope keeps its bits; the last four bytes are zero
+    x = np.zeros((1, 512), dtype=np.float32)
+    want = np.zeros(448, dtype=np.uint8)
+    for blk in range(6):
+        x[0, 64 * blk] = 448.0 * 2.0 ** -blk
+        x[0, 64 * blk + 1] = -224.0 * 2.0 ** -blk
+        want[64 * blk], want[64 * blk + 1] = 0x7E, 0xF6
+    x[0, 448:] = np.arange(-32, 32, dtype=np.float32) / 8.0
+    bits = _bf16_bits(x)
+    raw = O.pack_fp8_rows(bits)[0]
+    assert raw.shape == (608,)
+    assert np.array_equal(raw[:448], want)
+    assert np.array_equal(raw[448:576], bits[0, 448:].astype("<u2").view(np.uint8))
+    assert raw[576:604].copy().view("<f4").tolist() == [1.0, 0.5, 0.25, 0.125, 0.0625, 0.03125, 1.0]
+    assert raw[604:].tolist() == [0, 0, 0, 0]
+
+
+def pin_fp8_pack_library():
+    # random rows with blocks of very different magnitudes (down into the
+    # subnormal codes), zero blocks and negative zeros, against torch
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn(96, 512, generator=g) * 0.5
+    mag = torch.exp2(torch.randint(-20, 6, (96, 8), generator=g).float())
+    x = x * mag.repeat_interleave(64, dim=1)
+    x[5, 64:128] = 0.0
+    x[6, :] = -0.0
+    x[7, 0:64] = torch.tensor([1e-30] + [0.0] * 63)
+    bits = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.pack_fp8_rows(bits), _torch_pack_fp8(bits))
+
+
+def pin_kv_store_round_trip():
+    # The worked example's requests (request-pool rows 5 and 9): store the
+    # prefill rows and the decode step's new rows, then read every stored
+    # position back through the attention oracle (a one-key window and no
+    # sink returns that key exactly); rows that cannot be placed are skipped
+    # and reported, and nothing else in the pool changes.
+    g = _golden("request_mapping.txt")
+    rows5, rows9 = g["req_pool_indices"]
+    page_table = np.full((10, 4), -1, dtype=np.int32)
+    page_table[rows5] = [6, 1, 3, -1]
+    page_table[rows9] = [0, 7, -1, 2]
+    req, pos = [], []
+    for b, p in zip(g["prefill.requests"], g["prefill.positions"]):
+        req.append(g["req_pool_indices"][b])
+        pos.append(p)
+    for b, p in zip(g["decode.requests"], g["decode.positions"]):
+        req.append(g["req_pool_indices"][b])
+        pos.append(p)
+    req += [rows5, rows9, rows9]
+    pos += [511, 256, 1000]                       # logical pages 1, 1 and 3
+    bad_req = [rows5, rows9, 3, 10, rows5]
+    bad_pos = [-1, 520, 0, 0, 1024]               # negative, unmapped page, empty row, no row, past the table
+    rng = np.random.default_rng(5)
+    n = len(req) + len(bad_req)
+    vals = (rng.standard_normal((n, 512)) * 0.5).astype(np.float32)
+    bits = (vals.view(np.uint32) >> 16).astype(np.uint16)
+    req_all = np.array(req + bad_req, dtype=np.int32)
+    pos_all = np.array(pos + bad_pos, dtype=np.int32)
+    for fmt in ("bf16", "fp8"):
+        width = 512 if fmt == "bf16" else 608
+        dtype = np.uint16 if fmt == "bf16" else np.uint8
+        pool = rng.integers(0, 200, size=(8 * 256, width)).astype(dtype)
+        new, err = O.kv_store(pool, bits, req_all, pos_all, page_table, fmt)
+        assert err == O.ERR_STORE_ROW
+        changed = np.nonzero(np.any(new != pool, axis=1))[0]
+        assert len(changed) <= len(req)
+        for i, (r, p) in enumerate(zip(req, pos)):
+            res = O.dsv4_attention(np.zeros((1, 1, 512), dtype=np.uint16), np.array([-np.inf], np.float32), 1.0,
+                                   [p + 1], window=1, swa_pool=new, swa_page_table=page_table, kv_format=fmt,
+                                   req_pool_indices=[r])
+            want = O.bf16_bits_to_f64(bits[i]) if fmt == "bf16" else O.unpack_fp8_rows(O.pack_fp8_rows(bits[i:i + 1]))[0]
+            assert res.errors == 0 and np.array_equal(res.out[0, 0], want), (fmt, r, p)
+        _, err = O.kv_store(pool, bits[:len(req)], req_all[:len(req)], pos_all[:len(req)], page_table, fmt)
+        assert err == 0
 
 
 def pin_token_coordinates_golden():

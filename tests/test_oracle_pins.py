@@ -87,8 +87,51 @@ def _m_decode_shift(seq_lens, cu_seqlens_q=None):
     return req, (pos + 1 if cu_seqlens_q is None else pos)
 
 
+def _m_e4m3_truncate(x):
+    # rounds toward zero instead of to nearest
+    x = np.asarray(x, dtype=np.float32)
+    codes = _ENC(x)
+    up = O.e4m3_to_f64(codes & 0x7F) > np.abs(x.astype(np.float64))
+    return np.where(up & ((codes & 0x7F) > 0), codes - 1, codes).astype(np.uint8)
+
+
+def _m_pack_scale_447(bits):
+    bits = np.asarray(bits, dtype=np.uint16)
+    n = bits.shape[0]
+    x = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    nope = x[:, :448].reshape(n, 7, 64)
+    amax = np.max(np.abs(nope), axis=2)
+    scale = np.where(amax > 0, amax / np.float32(447.0), np.float32(1.0)).astype(np.float32)
+    out = _PACK(bits)
+    out[:, :448] = O.e4m3_from_f32((nope / scale[:, :, None]).astype(np.float32)).reshape(n, 448)
+    out[:, 576:604] = scale.astype("<f4").view(np.uint8).reshape(n, 28)
+    return out
+
+
+def _m_pack_rope_dropped(bits):
+    out = _PACK(bits)
+    out[:, 448:576] = 0
+    return out
+
+
+def _m_store_ignores_page(pool, bits, req_rows, positions, page_table, kv_format):
+    # writes logical row i of request row r at r * 256 + i % 256
+    out = np.array(pool, copy=True)
+    packed = O.pack_fp8_rows(bits) if kv_format == "fp8" else np.asarray(bits, dtype=np.uint16)
+    err = 0
+    for i in range(len(req_rows)):
+        r, p = int(req_rows[i]), int(positions[i])
+        if not (0 <= r < page_table.shape[0]) or O.physical_row(page_table, r, p, out.shape[0] // 256) < 0:
+            err |= O.ERR_STORE_ROW
+            continue
+        out[(r * 256 + p % 256) % out.shape[0]] = packed[i]
+    return out, err
+
+
 _ATTEND = O.attend
 _E4M3 = O.e4m3_to_f64
+_ENC = O.e4m3_from_f32
+_PACK = O.pack_fp8_rows
 _COORD = O.token_coordinates
 
 MUTANTS = {
@@ -104,6 +147,10 @@ MUTANTS = {
     "page_offset": ("physical_row", _m_page_offset),
     "verify_shift": ("token_coordinates", _m_verify_shift),
     "decode_shift": ("token_coordinates", _m_decode_shift),
+    "e4m3_truncate": ("e4m3_from_f32", _m_e4m3_truncate),
+    "pack_scale_447": ("pack_fp8_rows", _m_pack_scale_447),
+    "pack_rope_dropped": ("pack_fp8_rows", _m_pack_rope_dropped),
+    "store_ignores_page": ("kv_store", _m_store_ignores_page),
 }
 
 
