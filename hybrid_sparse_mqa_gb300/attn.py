@@ -9,7 +9,9 @@ no fallback path.
 The entry points mirror include/dsv4attn.h:
   dsv4_attn_swa, dsv4_attn_c4_sparse, dsv4_attn_c128_dense, dsv4_attn_verify,
   dsv4_attn_plan, dsv4_attn_workspace_size, dsv4_attn_get_device_error,
-  dsv4_attn_strerror.
+  dsv4_attn_strerror;
+and include/dsv4kvstore.h (the cache write before the step):
+  dsv4_kv_store.
 """
 from __future__ import annotations
 
@@ -26,12 +28,12 @@ DSV4_KV_BF16 = 0
 DSV4_KV_FP8_PACKED = 1
 DEV_ERR = {
     "SWA_PAGE": 0x01, "EXTRA_PAGE": 0x02, "INDEX_RANGE": 0x04, "POSITION": 0x08,
-    "PLAN": 0x10, "TIMEOUT": 0x20, "REQ_ROW": 0x40,
+    "PLAN": 0x10, "TIMEOUT": 0x20, "REQ_ROW": 0x40, "STORE_ROW": 0x80,
 }
 EXPORTED = [
     "dsv4_attn_swa", "dsv4_attn_c4_sparse", "dsv4_attn_c128_dense", "dsv4_attn_verify",
     "dsv4_attn_plan", "dsv4_attn_workspace_size", "dsv4_attn_get_device_error",
-    "dsv4_attn_strerror", "dsv4_attn_c4_sparse_noalloc",
+    "dsv4_attn_strerror", "dsv4_attn_c4_sparse_noalloc", "dsv4_kv_store",
 ]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -77,6 +79,8 @@ def load_library(path=LIB_PATH):
     lib.dsv4_attn_get_device_error.restype = ctypes.c_int
     lib.dsv4_attn_strerror.argtypes = [ctypes.c_int]
     lib.dsv4_attn_strerror.restype = ctypes.c_char_p
+    lib.dsv4_kv_store.argtypes = [P, I32, P, P, PP, P]
+    lib.dsv4_kv_store.restype = ctypes.c_int
     return lib
 
 
@@ -246,6 +250,20 @@ def dsv4_attn_strerror(status):
 
 
 # ---------------------------------------------------------------- one call per workload
+def dsv4_kv_store(k, req_rows, positions, pool, *, stream=None):
+    """Store new key rows k (bf16 [n, 512]) into `pool` (a make_pool()
+    descriptor) at logical row positions[i] of page-table row req_rows[i]
+    (int32 [n] each), packing them to FP8 for a packed pool."""
+    if k.dtype != torch.bfloat16 or k.dim() != 2 or k.shape[1] != 512 or not k.is_contiguous():
+        raise Dsv4Error("k must be a contiguous bf16 [n, 512] tensor")
+    n = k.shape[0]
+    for name, x in (("req_rows", req_rows), ("positions", positions)):
+        if x.dtype != torch.int32 or x.numel() != n or not x.is_contiguous():
+            raise Dsv4Error(f"{name} must be a contiguous int32 tensor of {n} entries")
+    _check(lib().dsv4_kv_store(_ptr(k), n, _ptr(req_rows), _ptr(positions), ctypes.byref(pool),
+                               _stream(stream)))
+
+
 def run_inputs(inp, *, num_splits=0, debug_rows=None, out=None, lse=None, workspace=None, stream=None):
     """Dispatch a synth.Inputs batch (already on the GPU) to the matching entry point."""
     w = inp.work

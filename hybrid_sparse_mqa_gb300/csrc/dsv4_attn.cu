@@ -41,6 +41,7 @@
 
 #include "dsv4attn.h"
 #include "dsv4_device.cuh"
+#include "dsv4_internal.h"
 
 namespace dsv4 {
 
@@ -1089,7 +1090,7 @@ static int make_plan(int T, int G, int lmax, int num_splits, const DeviceInfo& d
     return DSV4_OK;
 }
 
-static int check_pool(const dsv4_kv_pool* pool) {
+int check_pool(const dsv4_kv_pool* pool) {
     if (!pool || !pool->rows || !pool->page_table) return DSV4_ERR_INVALID;
     if (pool->page_size != kPageSize) return DSV4_ERR_UNSUPPORTED;
     if (pool->format == DSV4_KV_BF16) {
@@ -1103,6 +1104,24 @@ static int check_pool(const dsv4_kv_pool* pool) {
     if (pool->page_table_rows < 1 || pool->page_table_stride < 1) return DSV4_ERR_INVALID;
     if (reinterpret_cast<uintptr_t>(pool->rows) % 16) return DSV4_ERR_INVALID;
     return DSV4_OK;
+}
+
+static unsigned int* g_dev_error_addr[kMaxDevices];
+static std::mutex g_dev_error_mu;
+
+unsigned int* device_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_dev_error_mu);
+    if (g_dev_error_addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_dev_error) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_dev_error_addr[dev] = static_cast<unsigned int*>(ptr);
+    }
+    return g_dev_error_addr[dev];
 }
 
 // Workspace: [fp32 partial outputs and (m, l) of each cluster group when

@@ -248,6 +248,89 @@ def make_inputs(work: Workload | str, device="cpu", seed=None, **overrides) -> I
     return inp.to(dev)
 
 
+# --------------------------------------------------------------------------
+# Cache-write inputs: new key rows for a paged pool
+# --------------------------------------------------------------------------
+@dataclass(frozen=True)
+class StoreWorkload:
+    """`requests` requests each receive `rows_per_request` consecutive
+    logical rows starting at a random row below `max_len` (a prefill chunk;
+    one row per request is a decode step).  Request r uses page-table row
+    r * req_row_stride."""
+    name: str
+    requests: int
+    rows_per_request: int
+    kv_format: str = "fp8"
+    max_len: int = 65536
+    req_row_stride: int = 1
+    decoy_pages: int = 8
+    seed: int = 0
+
+    @property
+    def rows(self):
+        return self.requests * self.rows_per_request
+
+
+STORE_PRESETS = {
+    "kv_store_tiny": StoreWorkload("kv_store_tiny", requests=3, rows_per_request=341, max_len=4096,
+                                   req_row_stride=2, seed=21),
+    "kv_store_tiny_bf16": StoreWorkload("kv_store_tiny_bf16", requests=3, rows_per_request=341,
+                                        kv_format="bf16", max_len=4096, req_row_stride=2, seed=22),
+    "kv_store_prefill": StoreWorkload("kv_store_prefill", requests=64, rows_per_request=1024, seed=23),
+    "kv_store_decode": StoreWorkload("kv_store_decode", requests=64, rows_per_request=1, seed=24),
+}
+
+
+@dataclass
+class StoreInputs:
+    """One batch of new rows and the pool they go to (torch tensors)."""
+    work: StoreWorkload
+    k: torch.Tensor             # [n, 512] bf16
+    req_rows: torch.Tensor      # [n] int32
+    positions: torch.Tensor     # [n] int32
+    pool: torch.Tensor          # [rows, 608] uint8 or [rows, 512] bf16, random content
+    page_table: torch.Tensor    # [R, W] int32
+
+    def to(self, device):
+        return replace(self, k=self.k.to(device), req_rows=self.req_rows.to(device),
+                       positions=self.positions.to(device), pool=self.pool.to(device),
+                       page_table=self.page_table.to(device))
+
+    def oracle_kwargs(self):
+        def bits(x):
+            x = x.detach().cpu()
+            return x.view(torch.int16).numpy().view(np.uint16) if x.dtype == torch.bfloat16 else x.numpy()
+        return dict(pool=bits(self.pool), bits=bits(self.k), req_rows=self.req_rows.cpu().numpy(),
+                    positions=self.positions.cpu().numpy(), page_table=self.page_table.cpu().numpy(),
+                    kv_format=self.work.kv_format)
+
+
+def make_store_inputs(work: StoreWorkload | str, device="cpu", seed=None) -> StoreInputs:
+    """Draw new rows ~ N(0,1)*0.5 in bf16, their request rows and positions,
+    and a pool of randomly permuted pages (random content, so that a write
+    to the wrong row shows) covering every page the rows land on."""
+    if isinstance(work, str):
+        work = STORE_PRESETS[work]
+    if seed is not None:
+        work = replace(work, seed=seed)
+    gen_cpu = torch.Generator().manual_seed(work.seed)
+    dev = torch.device(device)
+    gen_dev = gen_cpu if dev.type == "cpu" else torch.Generator(device=dev).manual_seed(work.seed)
+    n_req, per = work.requests, work.rows_per_request
+    starts = torch.randint(0, work.max_len - per + 1, (n_req,), generator=gen_cpu).tolist()
+    table_rows = [r * work.req_row_stride for r in range(n_req)]
+    needed = []
+    for r in range(n_req):
+        needed += [(table_rows[r], lp) for lp in range(starts[r] // PAGE, (starts[r] + per - 1) // PAGE + 1)]
+    table, pages = _page_tables(needed, max(table_rows) + 1, work.max_len // PAGE, work.decoy_pages, gen_cpu)
+    pool = _pool(pages * PAGE, work.kv_format, gen_dev, dev)
+    req_rows = torch.tensor([table_rows[r] for r in range(n_req) for _ in range(per)], dtype=torch.int32)
+    positions = torch.tensor([starts[r] + i for r in range(n_req) for i in range(per)], dtype=torch.int32)
+    k = _randn_bf16((work.rows, DIM), gen_dev, dev)
+    return StoreInputs(work=work, k=k, req_rows=req_rows, positions=positions, pool=pool,
+                       page_table=table).to(dev)
+
+
 def _topk_lists(seq, qlen, topk, gen_cpu):
     """Per query token: min(topk, n_c) distinct uniform indices in [0, n_c(p)),
     unsorted, padded with -1 (n_c(p) = (p+1)//4 compressed rows are visible)."""

@@ -95,6 +95,8 @@ extern "C" {
 #define DSV4_DEV_ERR_PLAN         0x10u  /* key list longer than the split plan covers (max_seq_len too small) */
 #define DSV4_DEV_ERR_TIMEOUT      0x20u  /* an internal pipeline wait gave up (library bug) */
 #define DSV4_DEV_ERR_REQ_ROW      0x40u  /* req_pool_indices entry outside the page table */
+#define DSV4_DEV_ERR_STORE_ROW    0x80u  /* dsv4_kv_store (dsv4kvstore.h): a row whose request row,
+                                            logical page or page id is outside the tables or the pool */
 
 /* ---- KV pool formats ---- */
 #define DSV4_KV_BF16        0   /* row = 512 bf16 (1024 bytes) */

@@ -19,14 +19,19 @@ def A():
 
 
 def header_functions():
-    text = open(os.path.join(ROOT, "include", "dsv4attn.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(dsv4_attn_\w+)\s*\(", text)))
+    names = set()
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"\b(dsv4_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
     names = header_functions()
-    for want in ("dsv4_attn_swa", "dsv4_attn_c4_sparse", "dsv4_attn_c128_dense", "dsv4_attn_verify"):
+    for want in ("dsv4_attn_swa", "dsv4_attn_c4_sparse", "dsv4_attn_c128_dense", "dsv4_attn_verify",
+                 "dsv4_kv_store"):
         assert want in names
 
 
@@ -87,6 +92,29 @@ def test_host_validation(A):
     rc = lib.dsv4_attn_verify(4096, 2, 2, 64, 4096, None, None, ctypes.byref(ok), 128, 0, None, None,
                               0, 0, 4096, 0.044, 4096, None, 0, None, 0, None, None)
     assert rc == -1
+
+
+def test_kv_store_host_validation(A):
+    lib = A.lib()
+    ok = _pool(A)
+    fp8 = _pool(A, row_bytes=608, fmt=1)
+    assert lib.dsv4_kv_store(4096, -1, 4096, 4096, ctypes.byref(ok), None) == -1
+    assert lib.dsv4_kv_store(4096, 4, 4096, 4096, None, None) == -1
+    assert lib.dsv4_kv_store(4096, 4, 4096, 4096, ctypes.byref(_pool(A, page_size=128)), None) == -2
+    assert lib.dsv4_kv_store(4096, 4, 4096, 4096, ctypes.byref(_pool(A, row_bytes=1024, fmt=1)), None) == -2
+    assert lib.dsv4_kv_store(4096, 4, 4096, 4096, ctypes.byref(_pool(A, pages=0)), None) == -1
+    assert lib.dsv4_kv_store(None, 4, 4096, 4096, ctypes.byref(ok), None) == -1
+    assert lib.dsv4_kv_store(4096, 4, None, 4096, ctypes.byref(fp8), None) == -1
+    assert lib.dsv4_kv_store(4096, 4, 4096, None, ctypes.byref(fp8), None) == -1
+    assert lib.dsv4_kv_store(4104, 4, 4096, 4096, ctypes.byref(fp8), None) == -1     # k not 16-byte aligned
+    assert lib.dsv4_kv_store(None, 0, None, None, ctypes.byref(fp8), None) == 0       # nothing to store
+
+
+def test_kv_store_without_device_reports_cuda_error(A):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert A.lib().dsv4_kv_store(4096, 4, 4096, 4096, ctypes.byref(_pool(A, row_bytes=608, fmt=1)), None) == -4
 
 
 def test_plan_without_device_reports_cuda_error(A):
