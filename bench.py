@@ -5,6 +5,10 @@ One step = one call of the attention step over one batch of the workload
 Default workload: C4 top-512 decode, batch 32, H=64, D=512 bf16, context
 65536 (16384 compressed rows per request) + SWA window 128.
 
+`--workload kv_store_prefill` (or kv_store_decode) measures the cache write
+that precedes the step instead: one step = one dsv4_kv_store call packing and
+storing a batch of new key rows.
+
 Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs its own replica of the workload
@@ -32,6 +36,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "query-tokens/s and achieved HBM GB/s (% roofline) for C4 top-512 sparse MQA decode"
 DEFAULT_WORKLOAD = "c4_decode"
+STORE_METRIC = "KV rows stored/s and achieved HBM GB/s (% roofline) for the FP8 pack-and-store cache write"
 
 
 # ---------------------------------------------------------------- helpers
@@ -69,11 +74,15 @@ def measured_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
-def kernel_source_hash():
-    """Hash of the kernel sources' code: comments and whitespace do not count,
-    so a stored ncu figure stays valid until the code itself changes."""
+ATTN_SOURCES = ("hybrid_sparse_mqa_gb300/csrc/dsv4_attn.cu", "hybrid_sparse_mqa_gb300/csrc/dsv4_device.cuh")
+STORE_SOURCES = ("hybrid_sparse_mqa_gb300/csrc/dsv4_kv_store.cu",)
+
+
+def kernel_source_hash(sources=ATTN_SOURCES):
+    """Hash of a kernel's sources' code: comments and whitespace do not
+    count, so a stored ncu figure stays valid until the code itself changes."""
     h = hashlib.sha256()
-    for rel in ("hybrid_sparse_mqa_gb300/csrc/dsv4_attn.cu", "hybrid_sparse_mqa_gb300/csrc/dsv4_device.cuh"):
+    for rel in sources:
         with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
@@ -83,15 +92,17 @@ def kernel_source_hash():
 
 
 def ncu_traffic(workload):
-    """DRAM bytes per launch of the main kernel from the committed ncu summary,
-    if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "dsv4_attn_kernel_traffic.json")
+    """DRAM bytes per launch of the workload's main kernel from the committed
+    ncu summary, if it was taken on the current kernel source; else None."""
+    store = is_store_workload(workload)
+    name = "dsv4_kv_store_kernel_traffic.json" if store else "dsv4_attn_kernel_traffic.json"
+    path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     ent = d.get(workload)
-    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash(STORE_SOURCES if store else ATTN_SOURCES):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -203,7 +214,60 @@ def algorithmic_bytes_and_flops(inp):
     return nbytes, flops
 
 
+def store_algorithmic_bytes(inp):
+    """Bytes one cache-write call must move: each new bf16 row read (1024),
+    each stored row written (604 for a packed row - the 4 padding bytes are
+    not counted - or 1024), its request row and position (8), and one
+    page-table entry per distinct (request row, logical page)."""
+    n = inp.k.shape[0]
+    row_out = 604 if inp.work.kv_format == "fp8" else 1024
+    pages = set(zip(inp.req_rows.cpu().tolist(), (inp.positions.cpu() // 256).tolist()))
+    return n * (1024 + row_out + 8) + 4 * len(pages)
+
+
+def is_store_workload(name):
+    return name.startswith("kv_store")
+
+
 # ---------------------------------------------------------------- reference arm (the oracle)
+def run_reference_store(args):
+    from hybrid_sparse_mqa_gb300 import synth
+    from oracle import dsv4_oracle as O
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    inp = synth.make_store_inputs(args.workload, device="cpu")
+    kw = inp.oracle_kwargs()
+    n = inp.k.shape[0]
+    per = min(n, args.ref_rows)
+    sl = lambda k: dict(kw, bits=kw["bits"][k:k + per], req_rows=kw["req_rows"][k:k + per],
+                        positions=kw["positions"][k:k + per])
+    O.kv_store(**sl(0))
+    for _ in range(args.warmup):
+        O.kv_store(**sl(0))
+    t0 = time.perf_counter()
+    done = 0
+    for k in range(args.steps):
+        start = (k * per) % max(1, n - per + 1)
+        O.kv_store(**sl(start))
+        done += per
+    dt = time.perf_counter() - t0
+    value = done / dt
+    line = {
+        "impl": "reference", "metric": STORE_METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "rows_per_step": per,
+                   "note": f"oracle sample: {per} of the {n} new rows per step"},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{args.steps} steps x {per} rows of {args.workload}"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def run_reference(args):
     import numpy as np
     import torch
@@ -241,6 +305,185 @@ def run_reference(args):
         "e2e": {"value": value, "unit": "query-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- our arm: cache write
+def run_store(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from hybrid_sparse_mqa_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    from hybrid_sparse_mqa_gb300 import attn, synth
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sets = [synth.make_store_inputs(args.workload, device=dev, seed=2000 * (rank + 1) + r)
+            for r in range(args.sets)]
+    pools = [attn.make_pool(s.pool, s.page_table) for s in sets]
+    inp0 = sets[0]
+    n = inp0.k.shape[0]
+    nbytes = store_algorithmic_bytes(inp0)
+    R = len(sets)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(k, s=stream):
+        i = k % R
+        attn.dsv4_kv_store(sets[i].k, sets[i].req_rows, sets[i].positions, pools[i], stream=s)
+
+    with torch.cuda.stream(stream):
+        for k in range(max(args.warmup, 1)):
+            step(k)
+    torch.cuda.synchronize()
+    if attn.dsv4_attn_get_device_error(stream) != 0:
+        raise RuntimeError("device error flags set during warm-up")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for k in range(R):
+            step(k, torch.cuda.current_stream())
+    full, rem = divmod(args.steps, R)
+    tail = None
+    if rem:
+        tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tail, stream=stream):
+            for k in range(rem):
+                step(k, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    if not args.quick:
+        clocks.start()
+        time.sleep(0.5)
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, int(0.5 / max(1e-6, 20e-6 * R)))):
+                graph.replay()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(full):
+            graph.replay()
+        if tail is not None:
+            tail.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks.mark()
+    clocks.stop()
+    ms = slowest_ms(ev0.elapsed_time(ev1), world, dev)
+    flags = attn.dsv4_attn_get_device_error(stream)
+    sec_per_step = ms / 1e3 / args.steps
+    value = job_tokens_per_s(n, world, sec_per_step)
+
+    # ---- end to end: the new rows and their indices from pinned host memory,
+    # the store, and the first stored row read back
+    pin = lambda x: x.cpu().pin_memory()
+    hk = [pin(s.k) for s in sets]
+    hreq = [pin(s.req_rows) for s in sets]
+    hpos = [pin(s.positions) for s in sets]
+    first = []
+    for s in sets:
+        r, p0 = int(s.req_rows[0]), int(s.positions[0])
+        first.append(int(s.page_table[r, p0 // 256]) * 256 + p0 % 256)
+    hrow = [torch.empty(s.pool.shape[1:], dtype=s.pool.dtype, pin_memory=True) for s in sets]
+    h2d = hk[0].numel() * 2 + hreq[0].numel() * 4 + hpos[0].numel() * 4
+    d2h = hrow[0].numel() * hrow[0].element_size()
+
+    def e2e_step(k):
+        i = k % R
+        s = sets[i]
+        s.k.copy_(hk[i], non_blocking=True)
+        s.req_rows.copy_(hreq[i], non_blocking=True)
+        s.positions.copy_(hpos[i], non_blocking=True)
+        attn.dsv4_kv_store(s.k, s.req_rows, s.positions, pools[i], stream=stream)
+        hrow[i].copy_(s.pool[first[i]], non_blocking=True)
+
+    e2e_steps = min(args.steps, args.e2e_steps)
+    with torch.cuda.stream(stream):
+        for k in range(3):
+            e2e_step(k)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for k in range(e2e_steps):
+            e2e_step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ems = slowest_ms(e0.elapsed_time(e1), world, dev)
+    e2e_value = job_tokens_per_s(n, world, ems / 1e3 / e2e_steps)
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
+        from oracle import dsv4_oracle as O
+        kw = sets[0].oracle_kwargs()
+        per = min(n, args.ref_rows)
+        sub = dict(kw, bits=kw["bits"][:per], req_rows=kw["req_rows"][:per], positions=kw["positions"][:per])
+        O.kv_store(**sub)
+        t0 = time.perf_counter()
+        done = 0
+        while time.perf_counter() - t0 < args.cpu_seconds:
+            O.kv_store(**sub)
+            done += per
+        dt = time.perf_counter() - t0
+        cpu_baseline = {"value": done / dt, "unit": "rows/s", "cores": os.cpu_count(), "kind": "oracle",
+                        "sample": f"{done // per} oracle calls of {per} rows of {args.workload}, {dt:.1f} s, "
+                                  f"numpy (pack vectorised, placement one row at a time)"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    peaks = measured_peaks()
+    achieved = nbytes / sec_per_step / 1e9
+    w = inp0.work
+    line = {
+        "metric": STORE_METRIC,
+        "value": value,
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": sec_per_step * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "rows": n, "requests": w.requests,
+                   "rows_per_request": w.rows_per_request, "kv_format": w.kv_format, "input_sets": R,
+                   "l2": f"inputs larger than L2: {R} rotating sets with their own pools "
+                         f"({R * nbytes / 1e6:.0f} MB touched per rotation vs L2 {l2 / 1e6:.0f} MB)",
+                   "timing": "CUDA graph replays of one call per input set, CUDA events on the launch stream"},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(args.workload),
+                     "peak_source": peaks["source"], "algorithmic_bytes_per_launch": nbytes,
+                     "us_per_launch": sec_per_step * 1e6},
+        "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "cpu_baseline": cpu_baseline,
+        "clocks": clocks.summary(),
+        "device_error_flags": flags,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
     return 0
 
 
@@ -451,10 +694,14 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-tokens", type=int, default=8)
+    ap.add_argument("--ref-rows", type=int, default=4096,
+                    help="rows per oracle call for the cache-write workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="no clock sampling, no CPU baseline (for profiler runs)")
     args = ap.parse_args()
+    if is_store_workload(args.workload):
+        return run_reference_store(args) if args.impl == "reference" else run_store(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
