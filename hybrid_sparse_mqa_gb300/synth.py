@@ -331,6 +331,60 @@ def make_store_inputs(work: StoreWorkload | str, device="cpu", seed=None) -> Sto
                        page_table=table).to(dev)
 
 
+# --------------------------------------------------------------------------
+# Top-k selection inputs: indexer scores per query token
+# --------------------------------------------------------------------------
+@dataclass(frozen=True)
+class TopkWorkload:
+    """`rows` query tokens, each with `length` candidate scores (or the
+    given per-row lengths), fp32 ~ N(0,1); rows listed in `repeat_rows`
+    draw their scores from 64 values only, so many scores repeat."""
+    name: str
+    rows: int
+    length: int = 0
+    lengths: tuple | None = None
+    k: int = 512
+    repeat_rows: tuple = ()
+    seed: int = 0
+
+
+TOPK_PRESETS = {
+    "topk_tiny": TopkWorkload("topk_tiny", rows=6, lengths=(3000, 700, 512, 100, 2999, 513), k=512,
+                              repeat_rows=(4,), seed=41),
+    "topk_c4_decode": TopkWorkload("topk_c4_decode", rows=32, length=16384, seed=42),
+    "topk_1m": TopkWorkload("topk_1m", rows=32, length=262144, seed=43),
+}
+
+
+@dataclass
+class TopkInputs:
+    work: TopkWorkload
+    scores: torch.Tensor        # [rows, stride] fp32 (stride a multiple of 4)
+    lengths: torch.Tensor       # [rows] int32
+
+    def to(self, device):
+        return replace(self, scores=self.scores.to(device), lengths=self.lengths.to(device))
+
+    def oracle_kwargs(self):
+        return dict(scores=self.scores.cpu().numpy(), lengths=self.lengths.cpu().numpy(), k=self.work.k)
+
+
+def make_topk_inputs(work: TopkWorkload | str, device="cpu", seed=None) -> TopkInputs:
+    if isinstance(work, str):
+        work = TOPK_PRESETS[work]
+    if seed is not None:
+        work = replace(work, seed=seed)
+    lengths = list(work.lengths) if work.lengths is not None else [work.length] * work.rows
+    stride = max(4, (max(lengths) + 3) // 4 * 4)
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev).manual_seed(work.seed) if dev.type != "cpu" else \
+        torch.Generator().manual_seed(work.seed)
+    scores = torch.randn((work.rows, stride), generator=gen, device=dev, dtype=torch.float32)
+    for r in work.repeat_rows:
+        scores[r] = torch.randint(-32, 32, (stride,), generator=gen, device=dev).float() / 8.0
+    return TopkInputs(work=work, scores=scores, lengths=torch.tensor(lengths, dtype=torch.int32, device=dev))
+
+
 def _topk_lists(seq, qlen, topk, gen_cpu):
     """Per query token: min(topk, n_c) distinct uniform indices in [0, n_c(p)),
     unsorted, padded with -1 (n_c(p) = (p+1)//4 compressed rows are visible)."""

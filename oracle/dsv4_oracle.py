@@ -46,6 +46,11 @@ reads the cache; "SGLang DeepSeek-V4 Attention Test Capability Matrix",
 production pack-and-store path writes packed FP8 nope + BF16 rope rows, 584
 bytes per token, into the SWA and extra pools).
 
+It also states the top-k selection that produces the C4 index lists: for each
+query token, the indices of the k best of its indexer scores ("DeepSeek-V4 and
+SGLang Day-0", kernel list: at 1M context the indexer keeps the top 512 of
+256K candidate compressed rows, done by a radix select).
+
 Readings where the pages are silent (each is also listed in the design notes):
   R1 the current token is inside its own window: keys are positions
      max(0, p - window + 1) .. p;
@@ -66,6 +71,10 @@ Readings where the pages are silent (each is also listed in the design notes):
      to value / scale in float32 (ties to even; beyond 448 it saturates); the
      quantisation decision is taken in float32, the precision the writer
      computes in;
+  R15 top-k selection: scores are float32; a row's candidates are its first
+     `length` scores; they are ranked by value (-0 below +0, inputs finite),
+     equal values by lower index first; the output is the k best indices in
+     ascending index order, padded with -1 when length < k;
   R14 a new row goes to pool row page_table[r][i // 256] * 256 + i % 256 of
      its request row r, where i is its logical row number (the token position
      for the SWA pool, the compressed-row number for an extra pool); a row
@@ -339,6 +348,27 @@ def kv_store(pool, bits, req_rows, positions, page_table, kv_format):
             continue
         out[dest] = packed[i] if kv_format == "fp8" else bits[i]
     return out, errors
+
+
+def topk_indices(scores, lengths, k):
+    """Top-k selection for every row (reading R15).
+
+    scores: float32 [rows, >= max(lengths)]; lengths[r] candidates in row r.
+    Returns int32 [rows, k]: for each row, the indices of its k best scores
+    (by value, -0.0 ranked below +0.0, ties to the lower index), in
+    ascending index order, then -1 padding.
+    """
+    scores = np.asarray(scores, dtype=np.float32)
+    out = np.full((scores.shape[0], k), -1, dtype=np.int32)
+    for r in range(scores.shape[0]):
+        n = int(lengths[r])
+        row = scores[r, :n]
+        # the plain definition: sort the candidates by (value descending,
+        # index ascending) and keep the first k; -0.0 sorts below +0.0
+        order = sorted(range(n), key=lambda i: (-float(row[i]), 0 if np.signbit(row[i]) and row[i] == 0 else -1, i))
+        best = sorted(order[:k])
+        out[r, :len(best)] = best
+    return out
 
 
 def pool_rows_f64(pool, rows, kv_format):

@@ -338,6 +338,40 @@ def pin_kv_store_round_trip():
         assert err == 0
 
 
+def pin_topk_library():
+    # rows without repeated values: the selected set is torch.topk's; rows
+    # with repeats: the selected values are torch.topk's (as a multiset)
+    g = torch.Generator().manual_seed(23)
+    rows, n, k = 6, 3000, 128
+    x = torch.randn(rows, n, generator=g)
+    x[3] = torch.randint(-20, 20, (n,), generator=g).float()         # many repeats
+    x[4, :] = torch.linspace(-3, 3, n)
+    lengths = [n, n, 2000, n, n, 700]
+    got = O.topk_indices(x.numpy(), lengths, k)
+    for r in range(rows):
+        m = lengths[r]
+        vals, idx = torch.topk(x[r, :m], min(k, m))
+        sel = got[r][got[r] >= 0]
+        assert list(sel) == sorted(sel) and len(sel) == min(k, m)
+        assert np.array_equal(np.sort(x[r, sel].numpy()), np.sort(vals.numpy()))
+        if r != 3:
+            assert set(sel.tolist()) == set(idx.tolist())
+
+
+def pin_topk_closed_form():
+    # equal scores go to the lower index; fewer candidates than k pad with -1;
+    # +0.0 ranks above -0.0; a rising row keeps its last k
+    assert O.topk_indices(np.zeros((1, 10), np.float32), [10], 4).tolist() == [[0, 1, 2, 3]]
+    assert O.topk_indices(np.ones((1, 10), np.float32), [3], 5).tolist() == [[0, 1, 2, -1, -1]]
+    z = np.array([[-0.0, 0.0, -0.0, 0.0, -1.0]], dtype=np.float32)
+    assert O.topk_indices(z, [5], 3).tolist() == [[0, 1, 3]]
+    assert O.topk_indices(np.arange(50, dtype=np.float32)[None], [50], 5).tolist() == [[45, 46, 47, 48, 49]]
+    s = np.array([[0.5, -0.0, 0.0, 2.0, 2.0, -1.0, 0.0, 7.0]], np.float32)
+    assert O.topk_indices(s, [8], 4).tolist() == [[0, 3, 4, 7]]
+    assert O.topk_indices(s, [8], 6).tolist() == [[0, 2, 3, 4, 6, 7]]
+    assert O.topk_indices(s, [0], 2).tolist() == [[-1, -1]]
+
+
 def pin_token_coordinates_golden():
     g = _golden("request_mapping.txt")
     req, pos = O.token_coordinates(g["decode.seq_lens"])

@@ -128,7 +128,46 @@ def _m_store_ignores_page(pool, bits, req_rows, positions, page_table, kv_format
     return out, err
 
 
+def _m_topk_ties_high(scores, lengths, k):
+    # equal scores go to the higher index
+    scores = np.asarray(scores, dtype=np.float32)
+    out = np.full((scores.shape[0], k), -1, dtype=np.int32)
+    for r in range(scores.shape[0]):
+        n = int(lengths[r])
+        order = sorted(range(n), key=lambda i: (-float(scores[r, i]), -i))
+        best = sorted(order[:k])
+        out[r, :len(best)] = best
+    return out
+
+
+def _m_topk_score_order(scores, lengths, k):
+    # the best indices in score order instead of index order
+    out = _TOPK(scores, lengths, k)
+    scores = np.asarray(scores, dtype=np.float32)
+    for r in range(out.shape[0]):
+        sel = out[r][out[r] >= 0]
+        out[r, :len(sel)] = sel[np.argsort(-scores[r, sel], kind="stable")]
+    return out
+
+
+def _m_topk_zero_equal(scores, lengths, k):
+    # -0.0 and +0.0 treated as equal
+    scores = np.asarray(scores, dtype=np.float32)
+    out = np.full((scores.shape[0], k), -1, dtype=np.int32)
+    for r in range(scores.shape[0]):
+        n = int(lengths[r])
+        order = sorted(range(n), key=lambda i: (-float(scores[r, i]), i))
+        best = sorted(order[:k])
+        out[r, :len(best)] = best
+    return out
+
+
+def _m_topk_ignores_length(scores, lengths, k):
+    return _TOPK(scores, [np.asarray(scores).shape[1]] * len(lengths), k)
+
+
 _ATTEND = O.attend
+_TOPK = O.topk_indices
 _E4M3 = O.e4m3_to_f64
 _ENC = O.e4m3_from_f32
 _PACK = O.pack_fp8_rows
@@ -151,6 +190,10 @@ MUTANTS = {
     "pack_scale_447": ("pack_fp8_rows", _m_pack_scale_447),
     "pack_rope_dropped": ("pack_fp8_rows", _m_pack_rope_dropped),
     "store_ignores_page": ("kv_store", _m_store_ignores_page),
+    "topk_ties_high": ("topk_indices", _m_topk_ties_high),
+    "topk_score_order": ("topk_indices", _m_topk_score_order),
+    "topk_zero_equal": ("topk_indices", _m_topk_zero_equal),
+    "topk_ignores_length": ("topk_indices", _m_topk_ignores_length),
 }
 
 
