@@ -11,9 +11,11 @@ import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "dsv4_attn.cu"), os.path.join(PKG, "csrc", "dsv4_kv_store.cu")]
+SOURCES = [os.path.join(PKG, "csrc", "dsv4_attn.cu"), os.path.join(PKG, "csrc", "dsv4_kv_store.cu"),
+           os.path.join(PKG, "csrc", "dsv4_topk.cu")]
 DEPS = SOURCES + [os.path.join(PKG, "csrc", "dsv4_device.cuh"), os.path.join(PKG, "csrc", "dsv4_internal.h"),
-                  os.path.join(ROOT, "include", "dsv4attn.h"), os.path.join(ROOT, "include", "dsv4kvstore.h")]
+                  os.path.join(ROOT, "include", "dsv4attn.h"), os.path.join(ROOT, "include", "dsv4kvstore.h"),
+                  os.path.join(ROOT, "include", "dsv4topk.h")]
 LIB = os.path.join(PKG, "libdsv4attn.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

@@ -97,6 +97,7 @@ extern "C" {
 #define DSV4_DEV_ERR_REQ_ROW      0x40u  /* req_pool_indices entry outside the page table */
 #define DSV4_DEV_ERR_STORE_ROW    0x80u  /* dsv4_kv_store (dsv4kvstore.h): a row whose request row,
                                             logical page or page id is outside the tables or the pool */
+#define DSV4_DEV_ERR_TOPK_LENGTH  0x100u /* dsv4_topk (dsv4topk.h): a length outside 0..max_length */
 
 /* ---- KV pool formats ---- */
 #define DSV4_KV_BF16        0   /* row = 512 bf16 (1024 bytes) */

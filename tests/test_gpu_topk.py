@@ -1,0 +1,135 @@
+"""Top-k index selection (dsv4_topk, through the C ABI) against the oracle.
+
+The selected set is unique (ties go to the lower index, -0 ranks below +0)
+and the output order is ascending, so the bar is exact equality of the index
+lists.  At the 1M-context size the oracle checks sampled rows and every row
+is checked for the properties that define the result.
+"""
+import numpy as np
+import pytest
+import torch
+
+from hybrid_sparse_mqa_gb300 import synth
+from oracle import dsv4_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def A():
+    from hybrid_sparse_mqa_gb300 import build
+    build.build()
+    from hybrid_sparse_mqa_gb300 import attn
+    attn.lib()
+    attn.dsv4_attn_get_device_error()
+    return attn
+
+
+def run(A, scores, lengths, k, max_length=None, ws=None):
+    s = scores.cuda() if scores.device.type != "cuda" else scores
+    l = lengths.cuda() if lengths.device.type != "cuda" else lengths
+    out = A.dsv4_topk(s, l, k, max_length=max_length, workspace=ws)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), A.dsv4_attn_get_device_error()
+
+
+@pytest.mark.parametrize("name", ["topk_tiny", "topk_c4_decode"])
+def test_topk_matches_oracle(A, name):
+    inp = synth.make_topk_inputs(name)
+    got, flags = run(A, inp.scores, inp.lengths, inp.work.k)
+    assert flags == 0
+    assert np.array_equal(got, O.topk_indices(**inp.oracle_kwargs()))
+
+
+def test_topk_1m_context(A):
+    # 32 rows of 262144 candidates (the pages' 1M-context shape): rows 0, 13
+    # and 31 against the oracle; every row: 512 distinct ascending indices
+    # below the row length whose scores are exactly the 512 best values
+    inp = synth.make_topk_inputs("topk_1m", device="cuda")
+    k = inp.work.k
+    got, flags = run(A, inp.scores, inp.lengths, k)
+    assert flags == 0
+    kw = inp.oracle_kwargs()
+    for r in (0, 13, 31):
+        want = O.topk_indices(kw["scores"][r:r + 1], kw["lengths"][r:r + 1], k)[0]
+        assert np.array_equal(got[r], want), r
+    g = torch.from_numpy(got).cuda().long()
+    assert bool((g[:, 1:] > g[:, :-1]).all()) and bool((g >= 0).all())
+    assert bool((g < inp.lengths[:, None].long()).all())
+    best = torch.topk(inp.scores[:, :inp.lengths.max()], k, dim=1).values.sort(dim=1).values
+    assert torch.equal(torch.gather(inp.scores, 1, g).sort(dim=1).values, best)
+
+
+def test_topk_edges(A):
+    n = 40000
+    g = torch.Generator().manual_seed(9)
+    rows = []
+    rows.append(torch.zeros(n))                                       # all equal -> lowest indices
+    rows.append(torch.randn(n, generator=g))
+    z = torch.zeros(n)
+    z[torch.randperm(n, generator=g)[: n // 2]] = -0.0                # signed zeros
+    z[5], z[77] = -1.0, -2.0
+    rows.append(z)
+    rows.append(torch.randint(-3, 3, (n,), generator=g).float())      # heavy ties across chunks
+    rows.append(torch.arange(n).float())                              # rising: the last k
+    rows.append(-torch.arange(n).float())                             # falling: the first k
+    rows.append(torch.randn(n, generator=g))
+    rows.append(torch.randn(n, generator=g))
+    scores = torch.stack(rows)
+    lengths = torch.tensor([n, 16384, 16385, 32769, n, n, 0, 1], dtype=torch.int32)
+    for k in (1, 7, 512, 1024):
+        got, flags = run(A, scores, lengths, k)
+        assert flags == 0
+        assert np.array_equal(got, O.topk_indices(scores.numpy(), lengths.numpy(), k)), k
+
+
+def test_topk_length_out_of_range_is_clamped_and_reported(A):
+    scores = torch.randn(3, 2048)
+    lengths = torch.tensor([2048, 3000, -4], dtype=torch.int32)
+    got, flags = run(A, scores, lengths, 100, max_length=2048)
+    assert flags == 0x100
+    want = O.topk_indices(scores.numpy(), [2048, 2048, 0], 100)
+    assert np.array_equal(got, want)
+
+
+def test_topk_reuses_its_workspace(A):
+    # the per-row counters are left at zero: a second call on the same
+    # workspace (and a third with other scores) gives the right answer
+    inp = synth.make_topk_inputs("topk_1m", device="cuda")
+    rows = 4
+    scores, lengths = inp.scores[:rows].contiguous(), inp.lengths[:rows].contiguous()
+    ws = A.topk_workspace(rows, scores.shape[1], 512, "cuda")
+    a, _ = run(A, scores, lengths, 512, ws=ws)
+    b, _ = run(A, scores, lengths, 512, ws=ws)
+    assert np.array_equal(a, b)
+    c, flags = run(A, scores.flip(1).contiguous(), lengths, 512, ws=ws)
+    assert flags == 0
+    kw = dict(scores=scores.flip(1).cpu().numpy()[:1], lengths=lengths.cpu().numpy()[:1], k=512)
+    assert np.array_equal(c[:1], O.topk_indices(**kw))
+    assert int(ws.view(torch.int32)[-rows:].abs().sum()) == 0
+
+
+def test_topk_feeds_c4_attention(A):
+    # indexer scores -> top-512 -> C4 decode, on the GPU, against the oracle
+    # doing both steps
+    work = synth.Workload("topk_c4", batch=4, heads=64, ratio=4, seq_lens=(9000, 70000, 2500, 33000), seed=12)
+    inp = synth.make_inputs(work, device="cuda")
+    n_c = [(s) // 4 for s in work.seq_lens]                  # rows visible to the token at position s - 1
+    stride = (max(n_c) + 3) // 4 * 4
+    g = torch.Generator(device="cuda").manual_seed(3)
+    scores = torch.randn(work.batch, stride, generator=g, device="cuda")
+    lengths = torch.tensor(n_c, dtype=torch.int32, device="cuda")
+    idx = A.dsv4_topk(scores, lengths, 512)
+    inp.topk_idx = idx
+    out, lse = A.run_inputs(inp)
+    torch.cuda.synchronize()
+    assert A.dsv4_attn_get_device_error() == 0
+    want_idx = O.topk_indices(scores.cpu().numpy(), n_c, 512)
+    assert np.array_equal(idx.cpu().numpy(), want_idx)
+    kw = inp.oracle_kwargs()
+    kw["topk_idx"] = want_idx
+    res = O.dsv4_attention(**kw)
+    assert res.errors == 0
+    e = np.abs(out.float().cpu().numpy() - res.out)
+    assert e.max() <= 1e-2 and e.mean() <= 1e-3
+    assert np.abs(lse.cpu().numpy() - res.lse).max() <= 1e-3
