@@ -7,7 +7,9 @@ Default workload: C4 top-512 decode, batch 32, H=64, D=512 bf16, context
 
 `--workload kv_store_prefill` (or kv_store_decode) measures the cache write
 that precedes the step instead: one step = one dsv4_kv_store call packing and
-storing a batch of new key rows.
+storing a batch of new key rows.  `--workload topk_1m` (or topk_c4_decode)
+measures the top-k selection that makes the C4 index lists: one step = one
+dsv4_topk call over a batch of indexer score rows.
 
 Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -37,6 +39,7 @@ sys.path.insert(0, ROOT)
 METRIC = "query-tokens/s and achieved HBM GB/s (% roofline) for C4 top-512 sparse MQA decode"
 DEFAULT_WORKLOAD = "c4_decode"
 STORE_METRIC = "KV rows stored/s and achieved HBM GB/s (% roofline) for the FP8 pack-and-store cache write"
+TOPK_METRIC = "query-tokens/s (rows selected) and achieved HBM GB/s (% roofline) for top-k index selection"
 
 
 # ---------------------------------------------------------------- helpers
@@ -76,6 +79,7 @@ def measured_peaks():
 
 ATTN_SOURCES = ("hybrid_sparse_mqa_gb300/csrc/dsv4_attn.cu", "hybrid_sparse_mqa_gb300/csrc/dsv4_device.cuh")
 STORE_SOURCES = ("hybrid_sparse_mqa_gb300/csrc/dsv4_kv_store.cu",)
+TOPK_SOURCES = ("hybrid_sparse_mqa_gb300/csrc/dsv4_topk.cu",)
 
 
 def kernel_source_hash(sources=ATTN_SOURCES):
@@ -94,15 +98,19 @@ def kernel_source_hash(sources=ATTN_SOURCES):
 def ncu_traffic(workload):
     """DRAM bytes per launch of the workload's main kernel from the committed
     ncu summary, if it was taken on the current kernel source; else None."""
-    store = is_store_workload(workload)
-    name = "dsv4_kv_store_kernel_traffic.json" if store else "dsv4_attn_kernel_traffic.json"
+    if is_store_workload(workload):
+        name, sources = "dsv4_kv_store_kernel_traffic.json", STORE_SOURCES
+    elif is_topk_workload(workload):
+        name, sources = "dsv4_topk_kernel_traffic.json", TOPK_SOURCES
+    else:
+        name, sources = "dsv4_attn_kernel_traffic.json", ATTN_SOURCES
     path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     ent = d.get(workload)
-    if not ent or ent.get("kernel_source_hash") != kernel_source_hash(STORE_SOURCES if store else ATTN_SOURCES):
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash(sources):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -229,6 +237,17 @@ def is_store_workload(name):
     return name.startswith("kv_store")
 
 
+def is_topk_workload(name):
+    return name.startswith("topk")
+
+
+def topk_algorithmic_bytes(inp):
+    """Bytes one selection call must move: every candidate score read once
+    (4 bytes), the lengths, and the k output indices per row."""
+    lengths = inp.lengths.cpu().long()
+    return int(lengths.sum()) * 4 + 4 * inp.scores.shape[0] + 4 * inp.scores.shape[0] * inp.work.k
+
+
 # ---------------------------------------------------------------- reference arm (the oracle)
 def run_reference_store(args):
     from hybrid_sparse_mqa_gb300 import synth
@@ -262,6 +281,38 @@ def run_reference_store(args):
                    "note": f"oracle sample: {per} of the {n} new rows per step"},
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": f"{args.steps} steps x {per} rows of {args.workload}"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_reference_topk(args):
+    from hybrid_sparse_mqa_gb300 import synth
+    from oracle import dsv4_oracle as O
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    inp = synth.make_topk_inputs(args.workload, device="cpu")
+    kw = inp.oracle_kwargs()
+    rows = inp.scores.shape[0]
+    per = 1
+    O.topk_indices(kw["scores"][:1], kw["lengths"][:1], kw["k"])
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        r = s % rows
+        O.topk_indices(kw["scores"][r:r + 1], kw["lengths"][r:r + 1], kw["k"])
+    dt = time.perf_counter() - t0
+    value = args.steps * per / dt
+    line = {
+        "impl": "reference", "metric": TOPK_METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "config": {"workload": args.workload, "rows_per_step": per,
+                   "note": f"oracle sample: one of the {rows} rows per step"},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{args.steps} rows of {args.workload}, one per step"},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -487,6 +538,176 @@ def run_store(args):
     return 0
 
 
+# ---------------------------------------------------------------- our arm: top-k selection
+def run_topk(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from hybrid_sparse_mqa_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    from hybrid_sparse_mqa_gb300 import attn, synth
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sets = [synth.make_topk_inputs(args.workload, device=dev, seed=3000 * (rank + 1) + r) for r in range(args.sets)]
+    inp0 = sets[0]
+    rows, k = inp0.scores.shape[0], inp0.work.k
+    max_len = int(inp0.lengths.max())
+    nbytes = topk_algorithmic_bytes(inp0)
+    R = len(sets)
+    outs = [torch.empty(rows, k, dtype=torch.int32, device=dev) for _ in sets]
+    wss = [attn.topk_workspace(rows, max_len, k, dev) for _ in sets]
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, s=stream):
+        i %= R
+        attn.dsv4_topk(sets[i].scores, sets[i].lengths, k, max_length=max_len, out=outs[i], workspace=wss[i],
+                       stream=s)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 1)):
+            step(i)
+    torch.cuda.synchronize()
+    if attn.dsv4_attn_get_device_error(stream) != 0:
+        raise RuntimeError("device error flags set during warm-up")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(R):
+            step(i, torch.cuda.current_stream())
+    full, rem = divmod(args.steps, R)
+    tail = None
+    if rem:
+        tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tail, stream=stream):
+            for i in range(rem):
+                step(i, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    if not args.quick:
+        clocks.start()
+        time.sleep(0.5)
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, int(0.5 / max(1e-6, 10e-6 * R)))):
+                graph.replay()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(full):
+            graph.replay()
+        if tail is not None:
+            tail.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks.mark()
+    clocks.stop()
+    ms = slowest_ms(ev0.elapsed_time(ev1), world, dev)
+    flags = attn.dsv4_attn_get_device_error(stream)
+    sec_per_step = ms / 1e3 / args.steps
+    value = job_tokens_per_s(rows, world, sec_per_step)
+
+    # ---- end to end: scores and lengths from pinned host memory, the call,
+    # the index lists back to pinned host memory
+    hs = [s.scores.cpu().pin_memory() for s in sets]
+    hl = [s.lengths.cpu().pin_memory() for s in sets]
+    ho = [torch.empty(rows, k, dtype=torch.int32, pin_memory=True) for _ in sets]
+    h2d = hs[0].numel() * 4 + hl[0].numel() * 4
+    d2h = ho[0].numel() * 4
+
+    def e2e_step(i):
+        i %= R
+        sets[i].scores.copy_(hs[i], non_blocking=True)
+        sets[i].lengths.copy_(hl[i], non_blocking=True)
+        step(i)
+        ho[i].copy_(outs[i], non_blocking=True)
+
+    e2e_steps = min(args.steps, args.e2e_steps)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ems = slowest_ms(e0.elapsed_time(e1), world, dev)
+    e2e_value = job_tokens_per_s(rows, world, ems / 1e3 / e2e_steps)
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
+        from oracle import dsv4_oracle as O
+        kw = sets[0].oracle_kwargs()
+        O.topk_indices(kw["scores"][:1], kw["lengths"][:1], k)
+        t0 = time.perf_counter()
+        done = 0
+        while time.perf_counter() - t0 < args.cpu_seconds:
+            r = done % rows
+            O.topk_indices(kw["scores"][r:r + 1], kw["lengths"][r:r + 1], k)
+            done += 1
+        dt = time.perf_counter() - t0
+        cpu_baseline = {"value": done / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                        "sample": f"{done} rows of {args.workload}, one oracle call each, {dt:.1f} s "
+                                  f"(a Python sort per row: one core)"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    peaks = measured_peaks()
+    achieved = nbytes / sec_per_step / 1e9
+    line = {
+        "metric": TOPK_METRIC,
+        "value": value,
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": sec_per_step * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "rows": rows, "candidates_per_row": max_len, "k": k,
+                   "input_sets": R,
+                   "l2": f"inputs larger than L2: {R} rotating sets ({R * nbytes / 1e6:.0f} MB touched per "
+                         f"rotation vs L2 {l2 / 1e6:.0f} MB)",
+                   "timing": "CUDA graph replays of one call per input set, CUDA events on the launch stream"},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(args.workload),
+                     "peak_source": peaks["source"], "algorithmic_bytes_per_launch": nbytes,
+                     "us_per_launch": sec_per_step * 1e6},
+        "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "cpu_baseline": cpu_baseline,
+        "clocks": clocks.summary(),
+        "device_error_flags": flags,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args):
     import numpy as np
@@ -702,6 +923,8 @@ def main():
     args = ap.parse_args()
     if is_store_workload(args.workload):
         return run_reference_store(args) if args.impl == "reference" else run_store(args)
+    if is_topk_workload(args.workload):
+        return run_reference_topk(args) if args.impl == "reference" else run_topk(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
