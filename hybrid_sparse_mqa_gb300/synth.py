@@ -22,6 +22,8 @@ Shapes follow the five workloads of the step:
                  attended)
   c4_verify_fp8  batch 64 x 4 query tokens, H=64, context 262144, top-512,
                  packed FP8 KV
+  c4_prefill     batch 4 x 1024 query tokens (extend chunk), H=64, context
+                 65536, top-512
 Values: q and KV ~ N(0,1)*0.5 in bf16, sink ~ N(0,1) in fp32,
 scale = 1/sqrt(512).
 """
@@ -74,6 +76,9 @@ PRESETS = {
                             seq_lens=(1048576,) * 16, seed=3),
     "c4_verify_fp8": Workload("c4_verify_fp8", batch=64, heads=64, ratio=4,
                               seq_lens=(262144,) * 64, qlen=4, kv_format="fp8", seed=4),
+    # sparse prefill / extend: 4 requests each appending a 1024-token chunk at
+    # the end of a 65536-token context, C4 top-512 per query token
+    "c4_prefill": Workload("c4_prefill", batch=4, heads=64, ratio=4, seq_lens=(65536,) * 4, qlen=1024, seed=5),
 }
 
 

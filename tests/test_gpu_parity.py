@@ -101,6 +101,34 @@ def test_verify_small(attn, kind):
     run_and_compare(attn, small(kind, 64, (300, 1029, 5000), qlen=3, seed=30))
 
 
+@pytest.mark.parametrize("kind", ["swa", "c4", "c128"])
+def test_extend_chunks(attn, kind):
+    # sparse prefill / extend: requests appending chunks of 1..257 tokens,
+    # ragged, across page and window boundaries (every token checked)
+    work = synth.Workload(f"extend_{kind}", batch=3, heads=64, ratio={"swa": 0, "c4": 4, "c128": 128}[kind],
+                          seq_lens=(300, 2000, 9000), qlen=1, swa_resident="all", seed=33)
+    inp = synth.make_inputs(work)
+    # replace the one-token boundaries by ragged extend chunks of 257, 1 and 130 tokens
+    cu = torch.tensor([0, 257, 258, 388], dtype=torch.int32)
+    T = int(cu[-1])
+    g = torch.Generator().manual_seed(34)
+    inp.cu_seqlens_q = cu
+    inp.q = (torch.randn(T, 64, 512, generator=g) * 0.5).to(torch.bfloat16)
+    if work.ratio == 4:
+        seq = inp.seq_lens.tolist()
+        rows = []
+        for b, (lo, hi) in enumerate(zip(cu[:-1].tolist(), cu[1:].tolist())):
+            for i in range(hi - lo):
+                p = seq[b] - (hi - lo) + i
+                n_c = (p + 1) // 4
+                row = torch.full((512,), -1, dtype=torch.int32)
+                k = min(512, n_c)
+                row[:k] = torch.randperm(n_c, generator=g)[:k].to(torch.int32)
+                rows.append(row)
+        inp.topk_idx = torch.stack(rows)
+    run_and_compare(attn, inp)
+
+
 def test_req_pool_indices(attn):
     inp = small("c4", 32, (900, 3000), rpi=(5, 9), seed=40)
     run_and_compare(attn, inp)
@@ -144,6 +172,7 @@ def test_device_errors_are_flagged_not_trapped(attn):
     ("swa_decode", [0, 17, 40, 63]),
     ("c4_decode", [0, 9, 31]),
     ("c128_decode", [0, 15]),
+    ("c4_prefill", [0, 511, 1023, 1024, 2900, 4095]),
 ])
 def test_full_size_sampled(attn, name, tokens):
     inp = synth.make_inputs(name, device="cuda")
