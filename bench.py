@@ -563,13 +563,11 @@ def run_topk(args):
     nbytes = topk_algorithmic_bytes(inp0)
     R = len(sets)
     outs = [torch.empty(rows, k, dtype=torch.int32, device=dev) for _ in sets]
-    wss = [attn.topk_workspace(rows, max_len, k, dev) for _ in sets]
     stream = torch.cuda.Stream(device=dev)
 
     def step(i, s=stream):
         i %= R
-        attn.dsv4_topk(sets[i].scores, sets[i].lengths, k, max_length=max_len, out=outs[i], workspace=wss[i],
-                       stream=s)
+        attn.dsv4_topk(sets[i].scores, sets[i].lengths, k, max_length=max_len, out=outs[i], stream=s)
 
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 1)):

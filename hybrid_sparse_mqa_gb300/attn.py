@@ -13,7 +13,7 @@ The entry points mirror include/dsv4attn.h:
 include/dsv4kvstore.h (the cache write before the step):
   dsv4_kv_store;
 and include/dsv4topk.h (the top-k selection that makes the C4 index lists):
-  dsv4_topk, dsv4_topk_workspace_size, dsv4_topk_max_length.
+  dsv4_topk, dsv4_topk_max_length.
 """
 from __future__ import annotations
 
@@ -36,7 +36,7 @@ EXPORTED = [
     "dsv4_attn_swa", "dsv4_attn_c4_sparse", "dsv4_attn_c128_dense", "dsv4_attn_verify",
     "dsv4_attn_plan", "dsv4_attn_workspace_size", "dsv4_attn_get_device_error",
     "dsv4_attn_strerror", "dsv4_attn_c4_sparse_noalloc", "dsv4_kv_store",
-    "dsv4_topk", "dsv4_topk_workspace_size", "dsv4_topk_max_length",
+    "dsv4_topk", "dsv4_topk_max_length",
 ]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -84,10 +84,8 @@ def load_library(path=LIB_PATH):
     lib.dsv4_attn_strerror.restype = ctypes.c_char_p
     lib.dsv4_kv_store.argtypes = [P, I32, P, P, PP, P]
     lib.dsv4_kv_store.restype = ctypes.c_int
-    lib.dsv4_topk.argtypes = [P, I32, ctypes.c_int64, P, I32, I32, P, P, SZ, P]
+    lib.dsv4_topk.argtypes = [P, I32, ctypes.c_int64, P, I32, I32, P, P]
     lib.dsv4_topk.restype = ctypes.c_int
-    lib.dsv4_topk_workspace_size.argtypes = [I32, I32, I32]
-    lib.dsv4_topk_workspace_size.restype = SZ
     lib.dsv4_topk_max_length.argtypes = [I32]
     lib.dsv4_topk_max_length.restype = I32
     return lib
@@ -273,21 +271,11 @@ def dsv4_kv_store(k, req_rows, positions, pool, *, stream=None):
                                _stream(stream)))
 
 
-def dsv4_topk_workspace_size(num_rows, max_length, k):
-    return lib().dsv4_topk_workspace_size(num_rows, max_length, k)
-
-
 def dsv4_topk_max_length(k):
     return lib().dsv4_topk_max_length(k)
 
 
-def topk_workspace(num_rows, max_length, k, device):
-    """A workspace for dsv4_topk, zero-filled as the call requires before
-    first use (calls leave it zero-filled)."""
-    return torch.zeros(max(dsv4_topk_workspace_size(num_rows, max_length, k), 1), dtype=torch.uint8, device=device)
-
-
-def dsv4_topk(scores, lengths, k, *, max_length=None, out=None, workspace=None, stream=None):
+def dsv4_topk(scores, lengths, k, *, max_length=None, out=None, stream=None):
     """Indices of the k best scores of every row (ascending, -1 padded):
     scores fp32 [rows, stride] (stride a multiple of 4), lengths int32 [rows]."""
     if scores.dtype != torch.float32 or scores.dim() != 2 or scores.stride(1) != 1:
@@ -299,10 +287,8 @@ def dsv4_topk(scores, lengths, k, *, max_length=None, out=None, workspace=None, 
         max_length = scores.shape[1]
     if out is None:
         out = torch.empty(rows, k, dtype=torch.int32, device=scores.device)
-    if workspace is None:
-        workspace = topk_workspace(rows, max_length, k, scores.device)
     _check(lib().dsv4_topk(_ptr(scores), rows, scores.stride(0), _ptr(lengths), max_length, k, _ptr(out),
-                           _ptr(workspace), workspace.numel(), _stream(stream)))
+                           _stream(stream)))
     return out
 
 

@@ -4,27 +4,30 @@
 //
 // Sources (page title, section): "DeepSeek-V4 and SGLang Day-0" - kernel
 // list (the indexer keeps the top 512 of 256K candidates at 1M context with
-// a radix select over a thread-block cluster instead of a global sort);
+// a radix select over a cluster of thread blocks instead of a global sort);
 // "DeepSeek-V4 Attention: Query, Cache Write and History Addressing" -
 // section 5 (the top-k indices limit the C4 rows a token reads).
 //
 // How: a score's order-preserving 32-bit key (its fp32 bits with the sign
-// folded) makes "higher score" plain integer order.  A CTA takes a chunk of
-// 16384 scores of one row, 32 consecutive scores per thread held in
-// registers (one HBM read), and finds the k-th largest key by an exact radix
-// select: digits of 12, 10 and 10 bits from the top, counted into one shared
-// histogram (the first over the registers, the other two over a shared list
-// of the keys in the first digit's threshold bin), stopping as soon as the
-// k-th key's bin holds exactly the entries still needed.  Keys above the threshold are selected; when several
-// keys equal it, the lowest indices among them are taken, found by a prefix
-// count in index order (a thread's scores are consecutive, so thread order
-// is index order).  Selected entries leave in ascending index order through
-// one block-wide prefix sum.  A row of one chunk is done there; longer rows
-// write each chunk's k best (key and index) to the workspace, and the last
-// CTA of the row to finish (an atomic counter it resets) selects the final k
-// from those candidates the same way.  The pages' design spreads one row
-// over a cluster of 8 CTAs; here the chunks of a row need not be
-// co-resident, so any number of rows fills the GPU.
+// folded) makes "higher score" plain integer order.  One thread-block
+// cluster takes one row; CTA r of its C CTAs holds chunk r of the row on
+// chip (read once from HBM, coalesced), and the cluster finds the row's k-th
+// largest key by an exact radix select over digits of 12, 10 and 10 bits
+// from the top.  For each digit every CTA counts its keys into its own
+// shared histogram and adds the occupied bins into the totals of every CTA
+// of the cluster (distributed shared memory), so each CTA finds the bin
+// holding the k-th key by itself after one cluster barrier.  The select
+// stops as soon as that bin holds exactly the keys still needed.  One pass
+// over the keys after the first digit marks those above its bin and those
+// in it; the keys in the bin (few) go to a shared list that the later
+// digits are counted over.  Keys above the threshold are selected, keys
+// equal to it go to the lowest indices; per-warp counts, exchanged once
+// across the cluster, place every selected index at its rank in the row's
+// ascending order, so nothing is merged afterwards.
+//
+// Work per key is what bounds a long row (65536 keys per SM), so the per-key
+// passes are few and short: the count of the first digit, the marking pass,
+// and ballots over groups that hold a selection.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -32,428 +35,618 @@
 
 #include "dsv4attn.h"
 #include "dsv4topk.h"
+#include "dsv4_device.cuh"
 #include "dsv4_internal.h"
 
 namespace dsv4 {
 namespace {
 
-constexpr int kTkThreads = 512;
+constexpr int kTkThreads = 1024;
 constexpr int kTkWarps = kTkThreads / 32;
-constexpr int kKeysPerThread = 32;                        // scores per thread in a chunk
-constexpr int kChunk = kTkThreads * kKeysPerThread;       // 16384 scores per CTA
-constexpr int kMergePerThread = 16;                       // candidates per thread in a merge
-constexpr int kMergeCap = kTkThreads * kMergePerThread;   // 8192 candidates per row
+constexpr int kMaxClusterCtas = 8;                        // portable cluster size
+constexpr int kMaxKeys = 64;                              // scores per thread, longest chunk
+constexpr int kMaxLength = kMaxClusterCtas * kTkThreads * kMaxKeys;   // 524288
 constexpr int kMaxK = 1024;
-constexpr int kMaxChunks = 64;                            // chunks per row (size of the offset table)
+constexpr int kBins1 = 4096;                              // first digit: 12 bits
+constexpr int kBins2 = 1024;                              // second and third digits: 10 bits
+constexpr int kListCap = 8192;                            // threshold-bin keys a CTA lists
+constexpr int kAllEqual = 0x7fffffff;                     // every key equal to T is selected
 
 struct TopkParams {
     const float* scores;
     long long stride;          // floats between rows
     const int* lengths;
-    int rows;
     int max_len;
     int k;
-    int chunks;                // chunks of the longest row (grid x)
     int* out;                  // [rows][k]
-    unsigned long long* cand;  // [rows][chunks][k] composites of each chunk's k best
-    int* cnt;                  // [rows][chunks] how many each chunk kept
-    int* done;                 // [rows] chunks finished (zero between calls)
     unsigned int* err;
 };
 
-constexpr int kHistBins = 4096;                          // widest digit (12 bits)
-constexpr int kListCap = 8192;                            // keys of the threshold bin after the first digit
-
+// Per digit: this CTA's own counts (hist) and the cluster's totals (tot),
+// which every CTA of the cluster adds its occupied bins into.
 struct SelectSmem {
-    int hist[kHistBins];
+    int hist1[kBins1];
+    int hist2[kBins2];
+    int hist3[kBins2];
+    int tot1[kBins1];
+    int tot2[kBins2];
+    int tot3[kBins2];
     uint32_t list[kListCap];
-    int ctrl[3];
+    int cta_gt[kMaxClusterCtas];        // every CTA's count of keys above T
+    int cta_eq[kMaxClusterCtas];        // every CTA's count of keys equal to T
+    int warp_gt[kTkWarps];
+    int warp_eq[kTkWarps];
+    int ctrl[3];                        // threshold bin, entries above it, entries in it
+    int nlist;
     int wsum[kTkWarps];
-    int flag;
 };
 
-// fp32 bits -> uint32 whose unsigned order is the value order (-0 below +0)
 __device__ __forceinline__ uint32_t order_key(float f) {
     const uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return u ^ ((static_cast<uint32_t>(static_cast<int32_t>(u) >> 31)) | 0x80000000u);
+}
+// The float whose order key is k.
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
+__device__ __forceinline__ void red_cluster_add(uint32_t addr, int v) {
+    asm volatile("red.shared::cluster.add.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+// Sum of x (0 .. 7) over the lanes below this one, and over the warp.
+__device__ __forceinline__ int lane_prefix(int x, int& total) {
+    const uint32_t b0 = __ballot_sync(0xffffffffu, x & 1), b1 = __ballot_sync(0xffffffffu, x & 2),
+                   b2 = __ballot_sync(0xffffffffu, x & 4);
+    const uint32_t lt = lanemask_lt();
+    total = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
+    return __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
 }
 
-// Exclusive prefix sum of x over the block (thread order) and the total.
-__device__ int block_exclusive_scan(int x, int& total, SelectSmem& sm) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int v = x;
+// After this CTA has counted a digit into `hist` (BPT * kTkThreads bins,
+// thread t owning bins BPT*t .. BPT*t + BPT - 1): add its occupied bins into
+// `tot` of every CTA of the cluster, wait for the other CTAs' counts, and
+// find the bin holding the k_rem-th largest key of the row, leaving {bin,
+// entries above it, entries in it} in ctrl.
+template <int BPT>
+__device__ void cluster_find_bin(const int* hist, int* tot, int k_rem, int C, SelectSmem& sm) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int c[BPT];
+    if constexpr (BPT == 4) {
+        const int4 v = *reinterpret_cast<const int4*>(hist + 4 * tid);
+        c[0] = v.x;
+        c[1] = v.y;
+        c[2] = v.z;
+        c[3] = v.w;
+    } else {
+        c[0] = hist[tid];
+    }
+    const uint32_t a = smem_u32(tot + BPT * tid);
+#pragma unroll
+    for (int b = 0; b < BPT; ++b)
+        if (c[b])
+            for (int q = 0; q < C; ++q) red_cluster_add(mapa(a + 4u * b, q), c[b]);
+    cluster_sync();                                        // every CTA's counts are in tot
+    if constexpr (BPT == 4) {
+        const int4 v = *reinterpret_cast<const int4*>(tot + 4 * tid);
+        c[0] = v.x;
+        c[1] = v.y;
+        c[2] = v.z;
+        c[3] = v.w;
+    } else {
+        c[0] = tot[tid];
+    }
+    int mine = 0;
+#pragma unroll
+    for (int b = 0; b < BPT; ++b) mine += c[b];
+    int suf = mine;                                        // this lane's bins and every higher lane's
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off) v += y;
+        const int y = __shfl_down_sync(0xffffffffu, suf, off);
+        if (lane + off < 32) suf += y;
     }
-    if (lane == 31) sm.wsum[warp] = v;
+    if (lane == 0) sm.wsum[warp] = suf;
     __syncthreads();
-    int before = 0, tot = 0;
+    // entries in the bins of the warps above: lane l holds warp l's total
+    int ws = sm.wsum[lane];
 #pragma unroll
-    for (int w = 0; w < kTkWarps; ++w) {
-        const int s = sm.wsum[w];
-        before += w < warp ? s : 0;
-        tot += s;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, ws, off);
+        if (lane + off < 32) ws += y;
     }
-    total = tot;
-    __syncthreads();
-    return before + v - x;
-}
-
-// Histogram of digit (key >> shift) & (nb - 1) over the keys that match
-// `pval` on `pmask`, then the bin d holding the k_rem-th largest of them:
-// sets ctrl = {d, entries in bins above d, entries in bin d}.
-__device__ __forceinline__ int hist_total(const SelectSmem& sm, int b) { return sm.hist[b]; }
-__device__ __forceinline__ void hist_zero(SelectSmem& sm, int nb) {
-    for (int i = threadIdx.x; i < nb; i += kTkThreads) sm.hist[i] = 0;
-}
-
-__device__ void find_digit_bin(int nb, int k_rem, SelectSmem& sm) {
-    const int tid = threadIdx.x;
-    const int per = nb / kTkThreads;                 // bins owned by each thread
-    int own = 0;
-    for (int b = 0; b < per; ++b) own += hist_total(sm, tid * per + b);
-    int total;
-    const int before = block_exclusive_scan(own, total, sm);
-    int above = total - before - own;                // entries in the bins of later threads
-    for (int b = per - 1; b >= 0; --b) {
-        const int h = hist_total(sm, tid * per + b);
-        if (above < k_rem && above + h >= k_rem) {
-            sm.ctrl[0] = tid * per + b;
-            sm.ctrl[1] = above;
-            sm.ctrl[2] = h;
+    const int above_warps = __shfl_sync(0xffffffffu, ws, (warp + 1) & 31);
+    int ab = suf - mine + (warp + 1 < kTkWarps ? above_warps : 0);   // entries in bins above this thread's
+#pragma unroll
+    for (int b = BPT - 1; b >= 0; --b) {
+        if (ab < k_rem && ab + c[b] >= k_rem) {
+            sm.ctrl[0] = BPT * tid + b;
+            sm.ctrl[1] = ab;
+            sm.ctrl[2] = c[b];
         }
-        above += h;
+        ab += c[b];
     }
     __syncthreads();
 }
 
-// Threshold of the k largest keys among the block's valid entries (E per
-// thread, bit j of `valid` for entry j; at least k valid): every key above T
-// is selected, and `take_eq` of the keys equal to T (the lowest indices;
-// INT_MAX when all of them).  The first digit (12 bits) is counted over the
-// registers; the keys of its threshold bin are then gathered into a shared
-// list and the remaining two digits (10 bits each) are counted over it.
-template <int E>
-__device__ void select_threshold(const uint32_t (&key)[E], uint32_t valid, int k, uint32_t& T, int& take_eq,
-                                 SelectSmem& sm) {
-    const int tid = threadIdx.x;
-    int* hw = sm.hist;
-    // ---- digit 1: bits 31..20, over every key
-    hist_zero(sm, 4096);
-    __syncthreads();
+// The KPT scores one thread holds, in groups of four: group i of lane l in
+// warp w is scores wbase + 128 i + 4 l + 0..3 of the row (wbase: the warp's
+// first), so a warp reads 512 contiguous bytes per group.  Up to 8 groups
+// live as keys in registers; the rest (KPT = 64) as raw floats in shared
+// memory, group i of thread t at sk[(i - 8) * kTkThreads + t].  Groups
+// i < ng hold scores of the row; a key past the row's end is 0, below every
+// finite score's key.
+template <int KPT>
+struct Keys {
+    static constexpr int G = KPT / 4;
+    static constexpr int GR = G > 8 ? 8 : G;               // groups in registers
+    static constexpr int W = (KPT + 31) / 32;              // words of a per-key bit mask
+    uint32_t reg[4 * GR];
+    const float4* sk;
+    int ng;
+    // f(i, v): v the four keys of group i, for every group i < ng
+    template <class F>
+    __device__ __forceinline__ void for_each_group(F&& f) const {
 #pragma unroll
-    for (int j = 0; j < E; ++j)
-        if ((valid >> j) & 1u) atomicAdd(hw + (key[j] >> 20), 1);
-    __syncthreads();
-    find_digit_bin(4096, k, sm);
-    const int d1 = sm.ctrl[0];
-    int k_rem = k - sm.ctrl[1];
-    const int inbin1 = sm.ctrl[2];
-    uint32_t pval = static_cast<uint32_t>(d1) << 20;
-    if (inbin1 == k_rem) {
-        T = pval;
-        take_eq = 0x7fffffff;
-        return;
-    }
-    // ---- the bin's keys into the list (any order: only the threshold is
-    // sought); a bin too large for it is counted from the registers instead
-    const bool listed = inbin1 <= kListCap;
-    if (listed) {
-        uint32_t in = 0;
+        for (int i = 0; i < G; ++i) {
+            if (i < ng) {
+                uint32_t v[4];
+                if (i < GR) {
 #pragma unroll
-        for (int j = 0; j < E; ++j)
-            if (((valid >> j) & 1u) && (key[j] >> 20) == static_cast<uint32_t>(d1)) in |= 1u << j;
-        int total;
-        int o = block_exclusive_scan(__popc(in), total, sm);
-#pragma unroll
-        for (int j = 0; j < E; ++j)
-            if ((in >> j) & 1u) sm.list[o++] = key[j];
-    }
-    // ---- digits 2 and 3: bits 19..10, then 9..0
-    uint32_t pmask = 0xfff00000u;
-#pragma unroll 1
-    for (int shift = 10; shift >= 0; shift -= 10) {
-        hist_zero(sm, 1024);
-        __syncthreads();
-        if (listed) {
-            for (int i = tid; i < inbin1; i += kTkThreads) {
-                const uint32_t v = sm.list[i];
-                if ((v & pmask) == pval) atomicAdd(hw + ((v >> shift) & 1023u), 1);
+                    for (int c = 0; c < 4; ++c) v[c] = reg[4 * i + c];
+                } else {
+                    const float4 f4 = sk[(i - GR) * kTkThreads];
+                    v[0] = order_key(f4.x);
+                    v[1] = order_key(f4.y);
+                    v[2] = order_key(f4.z);
+                    v[3] = order_key(f4.w);
+                }
+                f(i, v);
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < E; ++j)
-                if (((valid >> j) & 1u) && (key[j] & pmask) == pval) atomicAdd(hw + ((key[j] >> shift) & 1023u), 1);
-        }
-        __syncthreads();
-        find_digit_bin(1024, k_rem, sm);
-        const int d = sm.ctrl[0], a = sm.ctrl[1], inbin = sm.ctrl[2];
-        k_rem -= a;
-        pval |= static_cast<uint32_t>(d) << shift;
-        pmask |= 1023u << shift;
-        if (inbin == k_rem) {
-            T = pval;
-            take_eq = 0x7fffffff;
-            return;
         }
     }
-    T = pval;                                        // the key is fully decided
-    take_eq = k_rem;
-}
-
-// Bit j set when entry j is among the k selected (threshold T, take_eq of
-// the keys equal to T in index order = thread order, then j).
-template <int E>
-__device__ uint32_t selected_mask(const uint32_t (&key)[E], uint32_t valid, uint32_t T, int take_eq,
-                                  SelectSmem& sm) {
-    uint32_t gt = 0, eq = 0;
+    // f(i, v) for the groups i < ng whose largest key may reach t (a
+    // superset of those that do: shared-memory groups are screened on their
+    // raw floats against t_f, the float of key t, or let through when that
+    // is not a number)
+    template <class F>
+    __device__ __forceinline__ void for_each_group_reaching(uint32_t t, float t_f, F&& f) const {
 #pragma unroll
-    for (int j = 0; j < E; ++j) {
-        if ((valid >> j) & 1u) {
-            gt |= (key[j] > T) ? (1u << j) : 0u;
-            eq |= (key[j] == T) ? (1u << j) : 0u;
+        for (int i = 0; i < G; ++i) {
+            if (i < ng) {
+                uint32_t v[4];
+                if (i < GR) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) v[c] = reg[4 * i + c];
+                    if (max(max(v[0], v[1]), max(v[2], v[3])) >= t) f(i, v);
+                } else {
+                    const float4 f4 = sk[(i - GR) * kTkThreads];
+                    if (!(fmaxf(fmaxf(f4.x, f4.y), fmaxf(f4.z, f4.w)) < t_f)) {
+                        v[0] = order_key(f4.x);
+                        v[1] = order_key(f4.y);
+                        v[2] = order_key(f4.z);
+                        v[3] = order_key(f4.w);
+                        f(i, v);
+                    }
+                }
+            }
         }
     }
-    if (take_eq == 0x7fffffff) return gt | eq;
-    int total;
-    int rank = block_exclusive_scan(__popc(eq), total, sm);   // equal keys before this thread's
-    uint32_t sel = gt;
-#pragma unroll
-    for (int j = 0; j < E; ++j)
-        if ((eq >> j) & 1u) {
-            if (rank < take_eq) sel |= 1u << j;
-            ++rank;
-        }
-    return sel;
-}
+    __device__ __forceinline__ static uint32_t nib(const uint32_t (&m)[W], int i) {
+        return (m[(4 * i) >> 5] >> ((4 * i) & 31)) & 0xfu;
+    }
+    // nib() for an index known only at run time
+    __device__ __forceinline__ static uint32_t nib_rt(const uint32_t (&m)[W], int i) {
+        uint32_t w = m[0];
+        if constexpr (W > 1) w = (4 * i >= 32) ? m[1] : w;
+        return (w >> ((4 * i) & 31)) & 0xfu;
+    }
+    __device__ __forceinline__ static void set_nib(uint32_t (&m)[W], int i, uint32_t x) {
+        m[(4 * i) >> 5] |= x << ((4 * i) & 31);
+    }
+};
 
 template <int KPT>
-__global__ void __launch_bounds__(kTkThreads, 2) dsv4_topk_kernel(const __grid_constant__ TopkParams p) {
-    constexpr int kCh = kTkThreads * KPT;                // scores per chunk
+__global__ void __launch_bounds__(kTkThreads, 1) dsv4_topk_kernel(const __grid_constant__ TopkParams p) {
+    using K = Keys<KPT>;
+    constexpr int kCh = kTkThreads * KPT;                  // scores per CTA
     extern __shared__ __align__(16) uint8_t tk_smem[];
     SelectSmem& sm = *reinterpret_cast<SelectSmem*>(tk_smem);
-    __shared__ int chunk_off[kMaxChunks + 1];
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int r = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+    const int C = static_cast<int>(gridDim.x);             // CTAs per row = the cluster
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int r = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int k = p.k;
     int n = __ldg(p.lengths + r);
     if (n < 0 || n > p.max_len) {
-        if (c == 0 && tid == 0) atomicOr(p.err, DSV4_DEV_ERR_TOPK_LENGTH);
+        if (rank == 0 && tid == 0) atomicOr(p.err, DSV4_DEV_ERR_TOPK_LENGTH);
         n = n < 0 ? 0 : p.max_len;
     }
     int* out = p.out + (size_t)r * k;
-    if (n <= k) {
-        // every candidate is selected
-        if (c == 0)
+    if (n <= k) {                                          // every candidate; the cluster leaves
+        if (rank == 0)
             for (int i = tid; i < k; i += kTkThreads) out[i] = i < n ? i : -1;
         return;
     }
-    const int nch = (n + kCh - 1) / kCh;
-    if (c >= nch) return;
-    const int base = c * kCh;
-    const int m = min(kCh, n - base);
-    const int first = KPT * tid;                 // this thread's scores: base + first + j
-    const uint32_t gidx0 = static_cast<uint32_t>(base + first);
-    const float* src = p.scores + (size_t)r * p.stride + base + first;
-    uint32_t key[KPT];
-    uint32_t valid = 0;
-    if (first + KPT <= m) {
-        const float4* s4 = reinterpret_cast<const float4*>(src);
+    // ---- this thread's scores: key (i, c) is row index wbase + 128 i + 4 lane + c
+    const int wbase = rank * kCh + warp * 32 * KPT;
+    const int lim = n - wbase - 4 * lane;                  // key (i, c) exists iff 128 i + c < lim
+    K key;
+    key.sk = reinterpret_cast<const float4*>(tk_smem + sizeof(SelectSmem)) + tid;
+    key.ng = lim <= 0 ? 0 : min(K::G, (lim + 127) / 128);
+    // a group's float4 never passes the row's stride (a multiple of 4 >= n)
+    const float4* src = reinterpret_cast<const float4*>(p.scores + (size_t)r * p.stride + wbase) + lane;
+    if constexpr (K::G > K::GR) {
+        // the shared-memory groups first, as asynchronous copies that stay
+        // in flight with the register loads below
+        const uint32_t dst = smem_u32(key.sk);
 #pragma unroll
-        for (int q = 0; q < KPT / 4; ++q) {
-            const float4 v = __ldcs(s4 + q);
-            key[4 * q] = order_key(v.x);
-            key[4 * q + 1] = order_key(v.y);
-            key[4 * q + 2] = order_key(v.z);
-            key[4 * q + 3] = order_key(v.w);
+        for (int i = K::GR; i < K::G; ++i)
+            if (i < key.ng) cp_async_16(dst + 16u * (i - K::GR) * kTkThreads, src + 32 * i, 16u);
+    }
+#pragma unroll
+    for (int i = 0; i < K::GR; ++i) {
+        uint32_t v[4] = {0u, 0u, 0u, 0u};
+        if (i < key.ng) {
+            const float4 f = __ldcs(src + 32 * i);
+            v[0] = order_key(f.x);
+            v[1] = order_key(f.y);
+            v[2] = order_key(f.z);
+            v[3] = order_key(f.w);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (128 * i + c >= lim) v[c] = 0u;
         }
-        valid = 0xffffffffu;
-    } else {
 #pragma unroll
-        for (int j = 0; j < KPT; ++j) {
-            key[j] = 0;
-            if (first + j < m) {
-                key[j] = order_key(__ldcs(src + j));
-                valid |= 1u << j;
-            }
-        }
+        for (int c = 0; c < 4; ++c) key.reg[4 * i + c] = v[c];
     }
-    const int want = min(k, m);
-    uint32_t sel = valid;
-    if (m > want) {
-        uint32_t T;
-        int take_eq;
-        select_threshold<KPT>(key, valid, want, T, take_eq, sm);
-        sel = selected_mask<KPT>(key, valid, T, take_eq, sm);
-    }
-    int total;
-    const int off = block_exclusive_scan(__popc(sel), total, sm);
-    if (nch == 1) {
-        // the whole row: its k indices, ascending
-        int o = off;
-#pragma unroll
-        for (int j = 0; j < KPT; ++j)
-            if ((sel >> j) & 1u) out[o++] = static_cast<int>(gidx0 + j);
-        return;
-    }
-    // this chunk's k best as (key << 32 | index), in index order
-    unsigned long long* cand = p.cand + ((size_t)r * p.chunks + c) * k;
     {
-        int o = off;
-#pragma unroll
-        for (int j = 0; j < KPT; ++j)
-            if ((sel >> j) & 1u) cand[o++] = (static_cast<unsigned long long>(key[j]) << 32) | (gidx0 + j);
+        int* z = sm.hist1;                                 // hist1 .. tot3 are contiguous
+        for (int i = tid; i < 2 * (kBins1 + 2 * kBins2); i += kTkThreads) z[i] = 0;
+        if (tid == 0) sm.nlist = 0;
     }
-    if (tid == 0) p.cnt[(size_t)r * p.chunks + c] = total;
-    // the last chunk of the row to finish selects among all chunks' candidates
-    __threadfence();
+    // the other CTAs add into this CTA's totals only once it has cleared them
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    if constexpr (K::G > K::GR) {
+        cp_async_wait_all();                               // this thread's own groups have landed
+        const int last = key.ng - 1;                       // a group cut by the row's end
+        if (last >= K::GR && 128 * last + 4 > lim) {
+            float* f = reinterpret_cast<float*>(tk_smem + sizeof(SelectSmem)) +
+                       4 * ((last - K::GR) * kTkThreads + tid);
+            for (int c = 0; c < 4; ++c)
+                if (128 * last + c >= lim) f[c] = __uint_as_float(0xffffffffu);   // key 0
+        }
+    }
     __syncthreads();
-    if (tid == 0) sm.flag = atomicAdd(p.done + r, 1) == nch - 1;
+
+    // ---- first digit, bits 31..20, over every key
+    key.for_each_group([&](int, const uint32_t(&v)[4]) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) atomicAdd(&sm.hist1[v[c] >> 20], 1);
+    });
     __syncthreads();
-    if (!sm.flag) return;
-    __threadfence();
-    if (tid < 32) {
-        // chunk counts loaded together (lanes l and l + 32), then prefix-summed
-        const int* cr = p.cnt + (size_t)r * p.chunks;
-        const int c0 = tid < nch ? __ldcg(cr + tid) : 0;
-        const int c1 = tid + 32 < nch ? __ldcg(cr + tid + 32) : 0;
-        int s0 = c0, s1 = c1;
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // every CTA's totals are cleared
+    cluster_find_bin<kBins1 / kTkThreads>(sm.hist1, sm.tot1, k, C, sm);
+    const uint32_t d1 = static_cast<uint32_t>(sm.ctrl[0]);
+    int k_rem = k - sm.ctrl[1];
+    const int inbin1 = sm.ctrl[2];
+    uint32_t pval = d1 << 20, pmask = 0xfff00000u;
+    uint32_t T = pval;
+    int take_eq = kAllEqual;
+    if (inbin1 != k_rem) {
+        // ---- this CTA's keys of the threshold bin into the list (any order);
+        // a bin too large for it (the same decision in every CTA) is counted
+        // from the keys themselves
+        const bool listed = inbin1 <= kListCap;
+        if (listed) {
+            uint32_t inm[K::W];
+#pragma unroll
+            for (int w = 0; w < K::W; ++w) inm[w] = 0u;
+            int cnt = 0;
+            key.for_each_group_reaching(pval, key_float(pval), [&](int i, const uint32_t(&v)[4]) {
+                uint32_t b = 0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) b |= static_cast<uint32_t>((v[c] & pmask) == pval) << c;
+                K::set_nib(inm, i, b);
+                cnt += __popc(b);
+            });
+            int wt, o;
+            {
+                int incl = cnt;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += y;
+                }
+                wt = __shfl_sync(0xffffffffu, incl, 31);
+                int wb = 0;
+                if (lane == 0 && wt) wb = atomicAdd(&sm.nlist, wt);
+                o = __shfl_sync(0xffffffffu, wb, 0) + incl - cnt;
+            }
+            if (cnt) {
+#pragma unroll
+                for (int i = 0; i < K::G; ++i) {
+                    const uint32_t b = K::nib(inm, i);
+                    if (b) {
+                        const float4 f4 = i < K::GR ? make_float4(0.f, 0.f, 0.f, 0.f) : key.sk[(i - K::GR) * kTkThreads];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            if ((b >> c) & 1u) {
+                                const uint32_t v = i < K::GR ? key.reg[(4 * i + c) % (4 * K::GR)]
+                                                             : order_key(c == 0 ? f4.x : c == 1 ? f4.y : c == 2 ? f4.z : f4.w);
+                                if (o < kListCap) sm.list[o] = v;
+                                ++o;
+                            }
+                    }
+                }
+            }
+            __syncthreads();
+        }
+        const int nlist = min(sm.nlist, kListCap);
+        // ---- digits 2 and 3: bits 19..10, then 9..0
+#pragma unroll 1
+        for (int d = 0; d < 2; ++d) {
+            const int shift = d == 0 ? 10 : 0;
+            int* hist = d == 0 ? sm.hist2 : sm.hist3;
+            int* tot = d == 0 ? sm.tot2 : sm.tot3;
+            if (listed) {
+                for (int i = tid; i < nlist; i += kTkThreads) {
+                    const uint32_t v = sm.list[i];
+                    if ((v & pmask) == pval) atomicAdd(&hist[(v >> shift) & 1023u], 1);
+                }
+            } else {
+                key.for_each_group_reaching(pval, key_float(pval), [&](int, const uint32_t(&v)[4]) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if ((v[c] & pmask) == pval) atomicAdd(&hist[(v[c] >> shift) & 1023u], 1);
+                });
+            }
+            __syncthreads();
+            cluster_find_bin<kBins2 / kTkThreads>(hist, tot, k_rem, C, sm);
+            k_rem -= sm.ctrl[1];
+            pval |= static_cast<uint32_t>(sm.ctrl[0]) << shift;
+            pmask |= 1023u << shift;
+            T = pval;
+            if (sm.ctrl[2] == k_rem) break;                // the whole bin is selected
+            if (d == 1) take_eq = k_rem;                   // T is a complete key
+        }
+    }
+    // ---- selection: keys above T, and the first take_eq keys equal to T in
+    // row order (kAllEqual: every key from T up); only groups whose largest
+    // key reaches T are looked at
+    uint32_t gt[K::W], eq[K::W], gsel = 0;                 // gsel: groups holding either
+#pragma unroll
+    for (int w = 0; w < K::W; ++w) gt[w] = eq[w] = 0u;
+    key.for_each_group_reaching(T, key_float(T), [&](int i, const uint32_t(&v)[4]) {
+        uint32_t g = 0, e = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            g |= static_cast<uint32_t>(v[c] > T) << c;
+            e |= static_cast<uint32_t>(v[c] == T) << c;
+        }
+        if (take_eq == kAllEqual) {
+            g |= e;
+            e = 0;
+        }
+        K::set_nib(gt, i, g);
+        K::set_nib(eq, i, e);
+        gsel |= static_cast<uint32_t>((g | e) != 0u) << i;
+    });
+    // ---- counts per warp, per CTA, and across the cluster
+    {
+        int gc = 0, ec = 0;
+#pragma unroll
+        for (int w = 0; w < K::W; ++w) {
+            gc += __popc(gt[w]);
+            ec += __popc(eq[w]);
+        }
+        gc = __reduce_add_sync(0xffffffffu, gc);
+        ec = __reduce_add_sync(0xffffffffu, ec);
+        if (lane == 0) {
+            sm.warp_gt[warp] = gc;
+            sm.warp_eq[warp] = ec;
+        }
+    }
+    __syncthreads();
+    int gb, eb, gtot, etot;                                // before this warp; in the CTA
+    {
+        // lane l holds warp l's counts: inclusive scans, read at this warp
+        int g = sm.warp_gt[lane], e = sm.warp_eq[lane];
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int y0 = __shfl_up_sync(0xffffffffu, s0, off), y1 = __shfl_up_sync(0xffffffffu, s1, off);
-            if (tid >= off) {
-                s0 += y0;
-                s1 += y1;
+            const int yg = __shfl_up_sync(0xffffffffu, g, off), ye = __shfl_up_sync(0xffffffffu, e, off);
+            if (lane >= off) {
+                g += yg;
+                e += ye;
             }
         }
-        const int tot0 = __shfl_sync(0xffffffffu, s0, 31);
-        chunk_off[tid] = s0 - c0;                  // exclusive offsets
-        chunk_off[tid + 32] = tot0 + s1 - c1;
-        if (tid == 31) chunk_off[64] = tot0 + s1;
-        if (tid == 0) p.done[r] = 0;             // ready for the next call
+        gtot = __shfl_sync(0xffffffffu, g, 31);
+        etot = __shfl_sync(0xffffffffu, e, 31);
+        const int gi = __shfl_sync(0xffffffffu, g, warp), ei = __shfl_sync(0xffffffffu, e, warp);
+        gb = gi - __shfl_sync(0xffffffffu, sm.warp_gt[lane], warp);
+        eb = ei - __shfl_sync(0xffffffffu, sm.warp_eq[lane], warp);
     }
-    __syncthreads();
-    const int ncand = chunk_off[nch];           // <= nch * k <= kMergeCap (host check on max_length)
-    const unsigned long long* rc = p.cand + (size_t)r * p.chunks * k;
-    uint32_t ck[kMergePerThread], ci[kMergePerThread];
-    uint32_t v2 = 0;
-    int cc = 0;
+    if (tid < C) {
+        st_cluster_s32(mapa(smem_u32(&sm.cta_gt[rank]), tid), gtot);
+        st_cluster_s32(mapa(smem_u32(&sm.cta_eq[rank]), tid), etot);
+    }
+    cluster_sync();                                        // every CTA's counts are everywhere
+    for (int q = 0; q < rank; ++q) {
+        gb += sm.cta_gt[q];
+        eb += sm.cta_eq[q];
+    }
+    // gb, eb: keys above T / equal to T before this warp in the row
+    int out_o = gb + min(eb, take_eq);                     // selected entries before this warp
+    int eq_rank = eb;
+    for (uint32_t wm = __reduce_or_sync(0xffffffffu, gsel); wm; wm &= wm - 1) {
+        const int i = __ffs(wm) - 1;                       // groups in ascending order
+        const uint32_t gn = K::nib_rt(gt, i), en = K::nib_rt(eq, i);
+        uint32_t tn = 0;                                   // equal keys taken
+        if (__any_sync(0xffffffffu, en != 0u)) {
+            int et;
+            int rk = eq_rank + lane_prefix(__popc(en), et);
 #pragma unroll
-    for (int j = 0; j < kMergePerThread; ++j) {
-        const int pos = kMergePerThread * tid + j;     // candidates in chunk order = ascending index
-        ck[j] = 0;
-        ci[j] = 0;
-        if (pos < ncand) {
-            while (chunk_off[cc + 1] <= pos) ++cc;
-            const unsigned long long v = __ldcg(rc + (size_t)cc * k + (pos - chunk_off[cc]));
-            ck[j] = static_cast<uint32_t>(v >> 32);
-            ci[j] = static_cast<uint32_t>(v);
-            v2 |= 1u << j;
+            for (int c = 0; c < 4; ++c)
+                if ((en >> c) & 1u) {
+                    tn |= static_cast<uint32_t>(rk < take_eq) << c;
+                    ++rk;
+                }
+            eq_rank += et;
         }
-    }
-    uint32_t sel2 = v2;
-    if (ncand > k) {
-        uint32_t T2;
-        int take_eq2;
-        select_threshold<kMergePerThread>(ck, v2, k, T2, take_eq2, sm);
-        sel2 = selected_mask<kMergePerThread>(ck, v2, T2, take_eq2, sm);
-    }
-    const int off2 = block_exclusive_scan(__popc(sel2), total, sm);
-    int o = off2;
+        const uint32_t sn = gn | tn;
+        int st;
+        int o = out_o + lane_prefix(__popc(sn), st);
 #pragma unroll
-    for (int j = 0; j < kMergePerThread; ++j)
-        if ((sel2 >> j) & 1u) out[o++] = static_cast<int>(ci[j]);
+        for (int c = 0; c < 4; ++c)
+            if ((sn >> c) & 1u) {
+                if (static_cast<unsigned>(o) < static_cast<unsigned>(k)) out[o] = wbase + 128 * i + 4 * lane + c;
+                ++o;
+            }
+        out_o += st;
+    }
 }
 
 std::mutex g_topk_mu;
-int g_topk_sms[64];
+int g_topk_sms[64];            // SM count per device, 0 until prepared
+int g_topk_clusters[64][5][kMaxClusterCtas + 1];   // clusters resident at once, per (device, KPT, size); 0 = not asked
 
-// The kernel's shared state exceeds the default 48 KB: allow it once per
-// device; returns the device's SM count (0 on failure).
-int topk_prepare_device() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    std::lock_guard<std::mutex> lock(g_topk_mu);
-    if (!g_topk_sms[dev]) {
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaFuncSetAttribute(dsv4_topk_kernel<kKeysPerThread>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(sizeof(SelectSmem))) != cudaSuccess) {
-            cudaGetLastError();
-            return 0;
-        }
-        g_topk_sms[dev] = sms;
-    }
-    return g_topk_sms[dev];
+constexpr int kKptCount = 5;                       // KPT = 4, 8, 16, 32, 64
+constexpr size_t topk_smem_bytes(int kpt) {
+    return sizeof(SelectSmem) + (kpt > 32 ? static_cast<size_t>(kpt - 32) * kTkThreads * 4 : 0);
+}
+static_assert(topk_smem_bytes(kMaxKeys) <= 227 * 1024, "top-k shared memory");
+
+template <int KPT>
+bool allow_smem() {
+    return cudaFuncSetAttribute(dsv4_topk_kernel<KPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(topk_smem_bytes(KPT))) == cudaSuccess;
 }
 
-size_t topk_ws_bytes(int rows, int max_len, int k) {
-    const size_t chunks = max_len > 0 ? (static_cast<size_t>(max_len) + kChunk - 1) / kChunk : 1;
-    return (static_cast<size_t>(rows) * chunks * k * 8 + 255) / 256 * 256 +
-           (static_cast<size_t>(rows) * chunks * 4 + 255) / 256 * 256 + static_cast<size_t>(rows) * 4;
+template <int KPT>
+cudaError_t launch_kpt(cudaLaunchConfig_t& cfg, const TopkParams& p, int* max_clusters) {
+    if (max_clusters) return cudaOccupancyMaxActiveClusters(max_clusters, dsv4_topk_kernel<KPT>, &cfg);
+    return cudaLaunchKernelEx(&cfg, dsv4_topk_kernel<KPT>, p);
+}
+
+// Launches (or, with max_clusters, asks how many clusters of this shape the
+// device holds at once).
+cudaError_t launch_topk(int kpt, cudaLaunchConfig_t& cfg, const TopkParams& p, int* max_clusters) {
+    switch (kpt) {
+        case 4: return launch_kpt<4>(cfg, p, max_clusters);
+        case 8: return launch_kpt<8>(cfg, p, max_clusters);
+        case 16: return launch_kpt<16>(cfg, p, max_clusters);
+        case 32: return launch_kpt<32>(cfg, p, max_clusters);
+        default: return launch_kpt<64>(cfg, p, max_clusters);
+    }
+}
+
+// The shared state exceeds the default 48 KB: allow it once per device.
+int topk_prepare_device(int& dev) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSV4_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_topk_mu);
+    if (!g_topk_sms[dev]) {
+        int n = 0;
+        if (!allow_smem<4>() || !allow_smem<8>() || !allow_smem<16>() || !allow_smem<32>() || !allow_smem<64>() ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            return DSV4_ERR_CUDA;
+        }
+        g_topk_sms[dev] = n;
+    }
+    return DSV4_OK;
+}
+
+void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int kpt, int C, int rows, cudaStream_t stream) {
+    cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(C), static_cast<unsigned>(rows), 1);
+    cfg.blockDim = dim3(kTkThreads, 1, 1);
+    cfg.dynamicSmemBytes = topk_smem_bytes(kpt);
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+}
+
+// Clusters of C CTAs at KPT scores per thread the device holds at once.
+int resident_clusters(int dev, int kpt_idx, int kpt, int C) {
+    {
+        std::lock_guard<std::mutex> lock(g_topk_mu);
+        if (g_topk_clusters[dev][kpt_idx][C]) return g_topk_clusters[dev][kpt_idx][C];
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fill_config(cfg, attr, kpt, C, 1, nullptr);
+    cfg.numAttrs = 1;                                      // the cluster shape alone
+    int n = 0;
+    TopkParams none = {};
+    if (launch_topk(kpt, cfg, none, &n) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = 1;
+    }
+    std::lock_guard<std::mutex> lock(g_topk_mu);
+    g_topk_clusters[dev][kpt_idx][C] = n;
+    return n;
 }
 
 }  // namespace
 }  // namespace dsv4
 
 extern "C" int32_t dsv4_topk_max_length(int32_t k) {
-    using namespace dsv4;
-    if (k < 1 || k > kMaxK) return 0;
-    const int chunks = kMergeCap / k < kMaxChunks ? kMergeCap / k : kMaxChunks;
-    return chunks * kChunk;
-}
-
-extern "C" size_t dsv4_topk_workspace_size(int32_t num_rows, int32_t max_length, int32_t k) {
-    if (num_rows < 1 || max_length < 0 || k < 1 || k > dsv4::kMaxK) return 0;
-    return dsv4::topk_ws_bytes(num_rows, max_length, k);
+    return (k < 1 || k > dsv4::kMaxK) ? 0 : dsv4::kMaxLength;
 }
 
 extern "C" int dsv4_topk(const float* scores, int32_t num_rows, int64_t row_stride, const int32_t* lengths,
-                         int32_t max_length, int32_t k, int32_t* out_idx, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+                         int32_t max_length, int32_t k, int32_t* out_idx, void* stream) {
     using namespace dsv4;
     if (num_rows < 1 || num_rows > 65535 || k < 1 || k > kMaxK || max_length < 0) return DSV4_ERR_INVALID;
     if (!scores || !lengths || !out_idx) return DSV4_ERR_INVALID;
     if (row_stride < max_length || row_stride % 4 || reinterpret_cast<uintptr_t>(scores) % 16) return DSV4_ERR_INVALID;
-    if (max_length > dsv4_topk_max_length(k)) return DSV4_ERR_UNSUPPORTED;
-    const size_t need = topk_ws_bytes(num_rows, max_length, k);
-    if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256) return DSV4_ERR_WORKSPACE;
+    if (max_length > kMaxLength) return DSV4_ERR_UNSUPPORTED;
     unsigned int* err = device_error_word();
     if (!err) return DSV4_ERR_CUDA;
-    if (!topk_prepare_device()) return DSV4_ERR_CUDA;
-    const int chunks = max_length > 0 ? (max_length + kChunk - 1) / kChunk : 1;
+    int dev = 0;
+    if (topk_prepare_device(dev) != DSV4_OK) return DSV4_ERR_CUDA;
+    // scores per thread: the fewest whose cluster (at most 8 CTAs) covers a
+    // row while every row's cluster is resident at once; failing that, the
+    // fewest that cover a row
+    const int len = max(max_length, 1);
+    int kpt = 0, C = 0;
+    for (int i = 0, e = 4; i < kKptCount; ++i, e *= 2) {
+        const int c = (len + kTkThreads * e - 1) / (kTkThreads * e);
+        if (c > kMaxClusterCtas) continue;
+        if (!kpt) {
+            kpt = e;
+            C = c;
+        }
+        if (num_rows <= resident_clusters(dev, i, e, c)) {
+            kpt = e;
+            C = c;
+            break;
+        }
+    }
     TopkParams p;
     p.scores = scores;
     p.stride = row_stride;
     p.lengths = lengths;
-    p.rows = num_rows;
     p.max_len = max_length;
     p.k = k;
-    p.chunks = chunks;
     p.out = out_idx;
-    uint8_t* w = static_cast<uint8_t*>(workspace);
-    p.cand = reinterpret_cast<unsigned long long*>(w);
-    w += (static_cast<size_t>(num_rows) * chunks * k * 8 + 255) / 256 * 256;
-    p.cnt = reinterpret_cast<int*>(w);
-    w += (static_cast<size_t>(num_rows) * chunks * 4 + 255) / 256 * 256;
-    p.done = reinterpret_cast<int*>(w);
     p.err = err;
-
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3(static_cast<unsigned>(chunks), static_cast<unsigned>(num_rows), 1);
-    cfg.blockDim = dim3(kTkThreads, 1, 1);
-    cfg.dynamicSmemBytes = sizeof(SelectSmem);
-    cfg.stream = static_cast<cudaStream_t>(stream);
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t le = cudaLaunchKernelEx(&cfg, dsv4_topk_kernel<kKeysPerThread>, p);
-    if (le != cudaSuccess) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fill_config(cfg, attr, kpt, C, num_rows, static_cast<cudaStream_t>(stream));
+    if (launch_topk(kpt, cfg, p, nullptr) != cudaSuccess) {
         cudaGetLastError();
         return DSV4_ERR_CUDA;
     }

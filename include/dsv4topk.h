@@ -24,23 +24,19 @@
  *               16-byte aligned.
  *   lengths:    int32 [num_rows], 0 <= lengths[r] <= max_length.
  *   max_length: bound on lengths (sizes the launch); at most
- *               dsv4_topk_max_length(k) (262144 for k = 512).
+ *               dsv4_topk_max_length(k) (524288).
  *   k:          1 .. 1024.
  *   out_idx:    int32 [num_rows, k].
- *   workspace:  dsv4_topk_workspace_size(num_rows, max_length, k) bytes,
- *               256-byte aligned, filled with zero bytes before its first
- *               use; every call leaves it that way again, so a buffer is
- *               zeroed once.
- *               Calls that can overlap on the GPU need separate buffers.
  *   stream:     a cudaStream_t (NULL = legacy default stream).
+ * The call needs no scratch memory: each row is held on chip by one
+ * thread-block cluster.
  *
  * Errors: DSV4_OK; DSV4_ERR_INVALID (null or misaligned pointer, num_rows
- * < 1, k outside 1..1024, max_length < 0, row_stride < max_length or not a
- * multiple of 4), DSV4_ERR_UNSUPPORTED (max_length above
- * dsv4_topk_max_length(k)), DSV4_ERR_WORKSPACE, DSV4_ERR_CUDA.  On the
- * device, a length outside 0..max_length is clamped into it and sets
- * DSV4_DEV_ERR_TOPK_LENGTH in the error word read by
- * dsv4_attn_get_device_error().
+ * outside 1..65535, k outside 1..1024, max_length < 0, row_stride <
+ * max_length or not a multiple of 4), DSV4_ERR_UNSUPPORTED (max_length above
+ * dsv4_topk_max_length(k)), DSV4_ERR_CUDA.  On the device, a length outside
+ * 0..max_length is clamped into it and sets DSV4_DEV_ERR_TOPK_LENGTH in the
+ * error word read by dsv4_attn_get_device_error().
  */
 #ifndef DSV4TOPK_H
 #define DSV4TOPK_H
@@ -54,11 +50,9 @@
 extern "C" {
 #endif
 
-size_t dsv4_topk_workspace_size(int32_t num_rows, int32_t max_length, int32_t k);
 int32_t dsv4_topk_max_length(int32_t k);
 int dsv4_topk(const float* scores, int32_t num_rows, int64_t row_stride, const int32_t* lengths,
-              int32_t max_length, int32_t k, int32_t* out_idx, void* workspace, size_t workspace_bytes,
-              void* stream);
+              int32_t max_length, int32_t k, int32_t* out_idx, void* stream);
 
 #ifdef __cplusplus
 }

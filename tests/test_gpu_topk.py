@@ -25,10 +25,10 @@ def A():
     return attn
 
 
-def run(A, scores, lengths, k, max_length=None, ws=None):
+def run(A, scores, lengths, k, max_length=None):
     s = scores.cuda() if scores.device.type != "cuda" else scores
     l = lengths.cuda() if lengths.device.type != "cuda" else lengths
-    out = A.dsv4_topk(s, l, k, max_length=max_length, workspace=ws)
+    out = A.dsv4_topk(s, l, k, max_length=max_length)
     torch.cuda.synchronize()
     return out.cpu().numpy(), A.dsv4_attn_get_device_error()
 
@@ -58,6 +58,23 @@ def test_topk_1m_context(A):
     assert bool((g < inp.lengths[:, None].long()).all())
     best = torch.topk(inp.scores[:, :inp.lengths.max()], k, dim=1).values.sort(dim=1).values
     assert torch.equal(torch.gather(inp.scores, 1, g).sort(dim=1).values, best)
+
+
+def test_topk_long_ragged_rows(A):
+    # 16 rows of up to 262144 candidates: the launch holds 64 scores per
+    # thread (half of them in shared memory) and rows end inside a group of
+    # four, inside the shared-memory half, at a CTA boundary and past it
+    rows, n = 16, 262144
+    g = torch.Generator().manual_seed(21)
+    scores = torch.randn(rows, n, generator=g)
+    scores[3, 70000:70600] = 5.0                                     # a tied block above the rest
+    scores[9] = torch.randint(-4, 4, (n,), generator=g).float()      # heavy ties
+    lengths = torch.tensor([n, n - 3, 200001, 131075, 65536, 65539, 40000, 513, 1025, 150002, 32768 + 34,
+                            32768 * 3 + 129, 262141, 99999, 7, 0], dtype=torch.int32)
+    for k in (512, 1024):
+        got, flags = run(A, scores, lengths, k)
+        assert flags == 0
+        assert np.array_equal(got, O.topk_indices(scores.numpy(), lengths.numpy(), k)), k
 
 
 def test_topk_edges(A):
@@ -92,21 +109,25 @@ def test_topk_length_out_of_range_is_clamped_and_reported(A):
     assert np.array_equal(got, want)
 
 
-def test_topk_reuses_its_workspace(A):
-    # the per-row counters are left at zero: a second call on the same
-    # workspace (and a third with other scores) gives the right answer
+def test_topk_repeated_and_back_to_back_calls(A):
+    # calls queued back to back on one stream (each may start while the one
+    # before drains) give the same answers as calls made one at a time
     inp = synth.make_topk_inputs("topk_1m", device="cuda")
     rows = 4
     scores, lengths = inp.scores[:rows].contiguous(), inp.lengths[:rows].contiguous()
-    ws = A.topk_workspace(rows, scores.shape[1], 512, "cuda")
-    a, _ = run(A, scores, lengths, 512, ws=ws)
-    b, _ = run(A, scores, lengths, 512, ws=ws)
-    assert np.array_equal(a, b)
-    c, flags = run(A, scores.flip(1).contiguous(), lengths, 512, ws=ws)
-    assert flags == 0
-    kw = dict(scores=scores.flip(1).cpu().numpy()[:1], lengths=lengths.cpu().numpy()[:1], k=512)
-    assert np.array_equal(c[:1], O.topk_indices(**kw))
-    assert int(ws.view(torch.int32)[-rows:].abs().sum()) == 0
+    flipped = scores.flip(1).contiguous()
+    a, _ = run(A, scores, lengths, 512)
+    outs = [A.dsv4_topk(x, lengths, 512) for x in (scores, flipped, scores, flipped)]
+    torch.cuda.synchronize()
+    assert A.dsv4_attn_get_device_error() == 0
+    kw = dict(scores=flipped.cpu().numpy()[:1], lengths=lengths.cpu().numpy()[:1], k=512)
+    want_flipped = O.topk_indices(**kw)[0]
+    for j, o in enumerate(outs):
+        o = o.cpu().numpy()
+        if j % 2 == 0:
+            assert np.array_equal(o, a)
+        else:
+            assert np.array_equal(o[0], want_flipped)
 
 
 def test_topk_feeds_c4_attention(A):

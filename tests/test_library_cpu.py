@@ -112,20 +112,20 @@ def test_kv_store_host_validation(A):
 
 def test_topk_host_validation(A):
     lib = A.lib()
-    ws = lambda rows, n, k: lib.dsv4_topk_workspace_size(rows, n, k)
-    assert lib.dsv4_topk_max_length(512) == 262144 and lib.dsv4_topk_max_length(0) == 0
-    assert ws(32, 262144, 512) > 32 * 16 * 512 * 8 and ws(0, 10, 5) == 0
-    big = 1 << 30
-    assert lib.dsv4_topk(4096, 0, 16, 4096, 16, 4, 4096, 4096, big, None) == -1          # no rows
-    assert lib.dsv4_topk(4096, 2, 16, 4096, 16, 0, 4096, 4096, big, None) == -1          # k = 0
-    assert lib.dsv4_topk(4096, 2, 16, 4096, 16, 1025, 4096, 4096, big, None) == -1       # k too large
-    assert lib.dsv4_topk(4096, 2, 14, 4096, 16, 4, 4096, 4096, big, None) == -1         # stride < max_length
-    assert lib.dsv4_topk(4096, 2, 18, 4096, 16, 4, 4096, 4096, big, None) == -1         # stride not a multiple of 4
-    assert lib.dsv4_topk(4100, 2, 16, 4096, 16, 4, 4096, 4096, big, None) == -1         # scores misaligned
-    assert lib.dsv4_topk(None, 2, 16, 4096, 16, 4, 4096, 4096, big, None) == -1
-    assert lib.dsv4_topk(4096, 2, 262148, 4096, 262148, 512, 4096, 4096, big, None) == -2   # too long
-    assert lib.dsv4_topk(4096, 2, 16, 4096, 16, 4, 4096, 4096, 8, None) == -3            # workspace too small
-    assert lib.dsv4_topk(4096, 2, 16, 4096, 16, 4, 4096, 4100, big, None) == -3          # workspace misaligned
+    assert lib.dsv4_topk_max_length(512) == 524288 and lib.dsv4_topk_max_length(1024) == 524288
+    assert lib.dsv4_topk_max_length(0) == 0 and lib.dsv4_topk_max_length(1025) == 0
+    assert lib.dsv4_topk(4096, 0, 16, 4096, 16, 4, 4096, None) == -1          # no rows
+    assert lib.dsv4_topk(4096, 65536, 16, 4096, 16, 4, 4096, None) == -1      # too many rows
+    assert lib.dsv4_topk(4096, 2, 16, 4096, 16, 0, 4096, None) == -1          # k = 0
+    assert lib.dsv4_topk(4096, 2, 16, 4096, 16, 1025, 4096, None) == -1       # k too large
+    assert lib.dsv4_topk(4096, 2, 16, 4096, -1, 4, 4096, None) == -1          # negative max_length
+    assert lib.dsv4_topk(4096, 2, 14, 4096, 16, 4, 4096, None) == -1          # stride < max_length
+    assert lib.dsv4_topk(4096, 2, 18, 4096, 16, 4, 4096, None) == -1          # stride not a multiple of 4
+    assert lib.dsv4_topk(4100, 2, 16, 4096, 16, 4, 4096, None) == -1          # scores misaligned
+    assert lib.dsv4_topk(None, 2, 16, 4096, 16, 4, 4096, None) == -1
+    assert lib.dsv4_topk(4096, 2, 16, None, 16, 4, 4096, None) == -1
+    assert lib.dsv4_topk(4096, 2, 16, 4096, 16, 4, None, None) == -1
+    assert lib.dsv4_topk(4096, 2, 524292, 4096, 524292, 512, 4096, None) == -2   # too long
 
 
 def test_kv_store_without_device_reports_cuda_error(A):
@@ -133,6 +133,13 @@ def test_kv_store_without_device_reports_cuda_error(A):
     if torch.cuda.is_available():
         pytest.skip("a device is present")
     assert A.lib().dsv4_kv_store(4096, 4, 4096, 4096, ctypes.byref(_pool(A, row_bytes=608, fmt=1)), None) == -4
+
+
+def test_topk_without_device_reports_cuda_error(A):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert A.lib().dsv4_topk(4096, 2, 16, 4096, 16, 4, 4096, None) == -4
 
 
 def test_plan_without_device_reports_cuda_error(A):
