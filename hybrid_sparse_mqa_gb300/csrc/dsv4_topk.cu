@@ -22,12 +22,14 @@
 // in it; the keys in the bin (few) go to a shared list that the later
 // digits are counted over.  Keys above the threshold are selected, keys
 // equal to it go to the lowest indices; per-warp counts, exchanged once
-// across the cluster, place every selected index at its rank in the row's
-// ascending order, so nothing is merged afterwards.
+// across the cluster, and a bitmap of each warp's positions place every
+// selected index at its rank in the row's ascending order, so nothing is
+// merged afterwards.
 //
 // Work per key is what bounds a long row (65536 keys per SM), so the per-key
-// passes are few and short: the count of the first digit, the marking pass,
-// and ballots over groups that hold a selection.
+// passes are few and short: the count of the first digit, then passes that
+// look only inside groups of four whose largest key reaches the bound.
+// Warp-wide instructions are counted too: all 32 warps issue them at once.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -95,20 +97,6 @@ __device__ __forceinline__ void red_cluster_add(uint32_t addr, int v) {
 __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
     asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ uint32_t lanemask_lt() {
-    uint32_t m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
-// Sum of x (0 .. 7) over the lanes below this one, and over the warp.
-__device__ __forceinline__ int lane_prefix(int x, int& total) {
-    const uint32_t b0 = __ballot_sync(0xffffffffu, x & 1), b1 = __ballot_sync(0xffffffffu, x & 2),
-                   b2 = __ballot_sync(0xffffffffu, x & 4);
-    const uint32_t lt = lanemask_lt();
-    total = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
-    return __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
-}
-
 // After this CTA has counted a digit into `hist` (BPT * kTkThreads bins,
 // thread t owning bins BPT*t .. BPT*t + BPT - 1): add its occupied bins into
 // `tot` of every CTA of the cluster, wait for the other CTAs' counts, and
@@ -239,12 +227,6 @@ struct Keys {
     }
     __device__ __forceinline__ static uint32_t nib(const uint32_t (&m)[W], int i) {
         return (m[(4 * i) >> 5] >> ((4 * i) & 31)) & 0xfu;
-    }
-    // nib() for an index known only at run time
-    __device__ __forceinline__ static uint32_t nib_rt(const uint32_t (&m)[W], int i) {
-        uint32_t w = m[0];
-        if constexpr (W > 1) w = (4 * i >= 32) ? m[1] : w;
-        return (w >> ((4 * i) & 31)) & 0xfu;
     }
     __device__ __forceinline__ static void set_nib(uint32_t (&m)[W], int i, uint32_t x) {
         m[(4 * i) >> 5] |= x << ((4 * i) & 31);
@@ -420,7 +402,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) dsv4_topk_kernel(const __grid_c
     // ---- selection: keys above T, and the first take_eq keys equal to T in
     // row order (kAllEqual: every key from T up); only groups whose largest
     // key reaches T are looked at
-    uint32_t gt[K::W], eq[K::W], gsel = 0;                 // gsel: groups holding either
+    uint32_t gt[K::W], eq[K::W];
 #pragma unroll
     for (int w = 0; w < K::W; ++w) gt[w] = eq[w] = 0u;
     key.for_each_group_reaching(T, key_float(T), [&](int i, const uint32_t(&v)[4]) {
@@ -436,7 +418,6 @@ __global__ void __launch_bounds__(kTkThreads, 1) dsv4_topk_kernel(const __grid_c
         }
         K::set_nib(gt, i, g);
         K::set_nib(eq, i, e);
-        gsel |= static_cast<uint32_t>((g | e) != 0u) << i;
     });
     // ---- counts per warp, per CTA, and across the cluster
     {
@@ -482,34 +463,84 @@ __global__ void __launch_bounds__(kTkThreads, 1) dsv4_topk_kernel(const __grid_c
         eb += sm.cta_eq[q];
     }
     // gb, eb: keys above T / equal to T before this warp in the row
-    int out_o = gb + min(eb, take_eq);                     // selected entries before this warp
-    int eq_rank = eb;
-    for (uint32_t wm = __reduce_or_sync(0xffffffffu, gsel); wm; wm &= wm - 1) {
-        const int i = __ffs(wm) - 1;                       // groups in ascending order
-        const uint32_t gn = K::nib_rt(gt, i), en = K::nib_rt(eq, i);
-        uint32_t tn = 0;                                   // equal keys taken
-        if (__any_sync(0xffffffffu, en != 0u)) {
-            int et;
-            int rk = eq_rank + lane_prefix(__popc(en), et);
+    const int out_o = gb + min(eb, take_eq);               // selected entries before this warp
+    // ---- write: the warp's selected positions (128 i + 4 lane + c within
+    // its region, which is row order) go to a bitmap of the region in the
+    // free list area, bit b of word b / 32 for position b; lane l then owns
+    // words 2l and 2l + 1 and one warp scan places every index.  With one
+    // group per lane the positions are in lane order already.
+    uint32_t a, b = 0u;                                    // the lane's selected positions, in order
+    int any_eq = 0;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                if ((en >> c) & 1u) {
-                    tn |= static_cast<uint32_t>(rk < take_eq) << c;
-                    ++rk;
-                }
-            eq_rank += et;
-        }
-        const uint32_t sn = gn | tn;
-        int st;
-        int o = out_o + lane_prefix(__popc(sn), st);
+    for (int w = 0; w < K::W; ++w) any_eq |= eq[w];
+    const bool weq = __any_sync(0xffffffffu, any_eq != 0);
+    if constexpr (K::G == 1) {
+        // one group: the lane's four positions 4 lane + c are already in row
+        // order, so a is its nibble (positions counted from 4 lane, below)
+        a = gt[0];
+        if (weq) {
+            uint32_t q = eq[0];
+            const int ec = __popc(q);
+            int incl = ec;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            if ((sn >> c) & 1u) {
-                if (static_cast<unsigned>(o) < static_cast<unsigned>(k)) out[o] = wbase + 128 * i + 4 * lane + c;
-                ++o;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
             }
-        out_o += st;
+            int rk = eb + incl - ec;
+            for (; q; q &= q - 1, ++rk)
+                if (rk < take_eq) a |= q & (0u - q);
+        }
+    } else {
+        uint32_t* bm = sm.list + warp * KPT;               // selected
+        uint32_t* bq = sm.list + (kTkWarps + warp) * KPT;  // equal to T (only when the warp has any)
+        for (int w = lane; w < KPT; w += 32) {
+            bm[w] = 0u;
+            if (weq) bq[w] = 0u;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < K::G; ++i) {
+            const uint32_t g = K::nib(gt, i), e = K::nib(eq, i);
+            const int wd = 4 * i + (lane >> 3), sh = 4 * (lane & 7);
+            if (g) atomicOr(&bm[wd], g << sh);
+            if (e) atomicOr(&bq[wd], e << sh);
+        }
+        __syncwarp();
+        const bool owns = 2 * lane < KPT;                  // words 2 lane, 2 lane + 1
+        a = owns ? bm[2 * lane] : 0u;
+        b = owns ? bm[2 * lane + 1] : 0u;
+        if (weq) {
+            // equal keys in row order take row ranks eb, eb + 1, ...: the
+            // first take_eq of the row are selected
+            uint32_t qa = owns ? bq[2 * lane] : 0u, qb = owns ? bq[2 * lane + 1] : 0u;
+            const int ec = __popc(qa) + __popc(qb);
+            int incl = ec;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            int rk = eb + incl - ec;
+            for (; qa; qa &= qa - 1, ++rk)
+                if (rk < take_eq) a |= qa & (0u - qa);
+            for (; qb; qb &= qb - 1, ++rk)
+                if (rk < take_eq) b |= qb & (0u - qb);
+        }
     }
+    const int sc = __popc(a) + __popc(b);
+    int incl = sc;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    int o = out_o + incl - sc;
+    const int pos0 = wbase + (K::G == 1 ? 4 : 64) * lane;
+    for (; a; a &= a - 1, ++o)
+        if (static_cast<unsigned>(o) < static_cast<unsigned>(k)) out[o] = pos0 + __ffs(a) - 1;
+    for (; b; b &= b - 1, ++o)
+        if (static_cast<unsigned>(o) < static_cast<unsigned>(k)) out[o] = pos0 + 32 + __ffs(b) - 1;
 }
 
 std::mutex g_topk_mu;
@@ -521,6 +552,7 @@ constexpr size_t topk_smem_bytes(int kpt) {
     return sizeof(SelectSmem) + (kpt > 32 ? static_cast<size_t>(kpt - 32) * kTkThreads * 4 : 0);
 }
 static_assert(topk_smem_bytes(kMaxKeys) <= 227 * 1024, "top-k shared memory");
+static_assert(2 * kTkWarps * kMaxKeys <= kListCap, "the output bitmaps reuse the list");
 
 template <int KPT>
 bool allow_smem() {

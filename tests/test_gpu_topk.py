@@ -77,6 +77,23 @@ def test_topk_long_ragged_rows(A):
         assert np.array_equal(got, O.topk_indices(scores.numpy(), lengths.numpy(), k)), k
 
 
+@pytest.mark.parametrize("rows,n", [(32, 16384), (8, 40000), (32, 65536), (8, 262144), (16, 262144)])
+def test_topk_ties_every_launch_shape(A, rows, n):
+    # integer-valued scores (long runs of equal values across warps, CTAs and
+    # the cluster) at lengths that select each launch shape: 4, 8, 16, 32 and
+    # 64 scores per thread; row lengths end inside a group of four
+    g = torch.Generator().manual_seed(rows * 7 + n)
+    scores = torch.randint(-6, 6, (rows, n), generator=g).float()
+    scores[0] = 1.0                                                  # one value everywhere
+    scores[1, n // 3:] = 7.0                                         # the top value in one late run
+    lengths = torch.full((rows,), n, dtype=torch.int32)
+    lengths[2::3] = torch.randint(n // 2, n, (len(range(2, rows, 3)),), generator=g, dtype=torch.int32)
+    for k in (512, 1000):
+        got, flags = run(A, scores, lengths, k)
+        assert flags == 0
+        assert np.array_equal(got, O.topk_indices(scores.numpy(), lengths.numpy(), k)), k
+
+
 def test_topk_edges(A):
     n = 40000
     g = torch.Generator().manual_seed(9)
