@@ -32,6 +32,7 @@
 // Warp-wide instructions are counted too: all 32 warps issue them at once.
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 #include <mutex>
 
@@ -82,6 +83,13 @@ struct SelectSmem {
     int nlist;
     int wsum[kTkWarps];
 };
+
+// The raw floats of the shared-memory key groups follow the select state:
+// their 16-byte copies and loads need it to end on a 16-byte boundary, and
+// the first digit's counts are read as int4.
+static_assert(sizeof(SelectSmem) % 16 == 0, "key groups follow the select state on a 16-byte boundary");
+static_assert(offsetof(SelectSmem, hist1) % 16 == 0 && offsetof(SelectSmem, tot1) % 16 == 0,
+              "first-digit counts are read as int4");
 
 __device__ __forceinline__ uint32_t order_key(float f) {
     const uint32_t u = __float_as_uint(f);
