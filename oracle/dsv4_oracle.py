@@ -66,20 +66,30 @@ Readings where the pages are silent (each is also listed in the design notes):
      scale per 64 nope values, stride 608 bytes;
   R8 e4m3 is the OCP FP8 E4M3 format (bias 7, subnormals, no infinities,
      S.1111.111 is NaN).
+  R9 in a verify (or extend) call, request b's query rows are its last
+     qlen_b positions, in order, and each sees keys up to its own position
+     ("DeepSeek-V4 Attention: Query, Cache Write and History Addressing",
+     section 4: cu_seqlens and positions);
+  R10 req_pool_indices maps a batch row to its page-table row (same page,
+     section 4, req_pool_indices = [5, 9]); without it the map is the
+     identity;
+  R11 the result is unique up to rounding: only the order of the sums is
+     free;
+  R12 the softmax scale is 1 / sqrt(512), the head dimension.
   R13 the packer's scale of a 64-value nope block is amax / 448 in float32
      (1 when the block is all zero) and each code is the e4m3 value nearest
      to value / scale in float32 (ties to even; beyond 448 it saturates); the
      quantisation decision is taken in float32, the precision the writer
      computes in;
-  R15 top-k selection: scores are float32; a row's candidates are its first
-     `length` scores; they are ranked by value (-0 below +0, inputs finite),
-     equal values by lower index first; the output is the k best indices in
-     ascending index order, padded with -1 when length < k;
   R14 a new row goes to pool row page_table[r][i // 256] * 256 + i % 256 of
      its request row r, where i is its logical row number (the token position
      for the SWA pool, the compressed-row number for an extra pool); a row
      whose request row, logical page or physical page is outside the tables
      or the pool is not written and is reported.
+  R15 top-k selection: scores are float32; a row's candidates are its first
+     `length` scores; they are ranked by value (-0 below +0, inputs finite),
+     equal values by lower index first; the output is the k best indices in
+     ascending index order, padded with -1 when length < k.
 
 Parity pins: every function here is pinned by the CPU tests against something
 other than itself (closed forms, brute force, textbook softmax, library e4m3
