@@ -17,11 +17,12 @@
 // shared histogram and adds the occupied bins into the totals of every CTA
 // of the cluster (distributed shared memory), so each CTA finds the bin
 // holding the k-th key by itself after one cluster barrier.  The select
-// stops as soon as that bin holds exactly the keys still needed.  One pass
-// over the keys after the first digit marks those above its bin and those
-// in it; the keys in the bin (few) go to a shared list that the later
-// digits are counted over.  Keys above the threshold are selected, keys
-// equal to it go to the lowest indices; per-warp counts, exchanged once
+// stops as soon as that bin holds exactly the keys still needed.  After the
+// first digit the keys of its bin (few) go to a shared list that the later
+// digits are counted over, and a last pass marks the keys above the
+// threshold T and those equal to it; both passes look only inside groups of
+// four keys whose largest reaches the bound.  Keys above T are selected,
+// keys equal to it go to the lowest indices; per-warp counts, exchanged once
 // across the cluster, and a bitmap of each warp's positions place every
 // selected index at its rank in the row's ascending order, so nothing is
 // merged afterwards.
