@@ -82,8 +82,9 @@ def test_swa_decode_boundaries(attn, heads):
 
 @pytest.mark.parametrize("heads", [16, 64, 128])
 def test_c4_decode_small(attn, heads):
-    # n_c(p) below and above topk (short lists are padded with -1 slots)
-    run_and_compare(attn, small("c4", heads, (4, 100, 515, 2048, 2049, 9000), seed=10 + heads))
+    # no compressed row visible yet (lengths 1 and 3: every index slot is
+    # absent), n_c(p) below and above topk (short lists are padded with -1)
+    run_and_compare(attn, small("c4", heads, (1, 3, 4, 100, 515, 2048, 2049, 9000), seed=10 + heads))
 
 
 @pytest.mark.parametrize("topk", [16, 100, 512])
