@@ -94,6 +94,21 @@ def test_topk_ties_every_launch_shape(A, rows, n):
         assert np.array_equal(got, O.topk_indices(scores.numpy(), lengths.numpy(), k)), k
 
 
+def test_topk_longest_rows(A):
+    # rows up to the longest length the call takes (524288: eight CTAs of
+    # 65536 scores per row), ragged, with a tied block near the end
+    n = A.dsv4_topk_max_length(512)
+    assert n == 524288
+    g = torch.Generator().manual_seed(23)
+    scores = torch.randn(4, n, generator=g)
+    scores[1, n - 700:n - 100] = 6.0
+    lengths = torch.tensor([n, n - 1, 300001, 65537], dtype=torch.int32)
+    for k in (512, 1024):
+        got, flags = run(A, scores, lengths, k)
+        assert flags == 0
+        assert np.array_equal(got, O.topk_indices(scores.numpy(), lengths.numpy(), k)), k
+
+
 def test_topk_edges(A):
     n = 40000
     g = torch.Generator().manual_seed(9)
