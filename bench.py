@@ -40,6 +40,7 @@ METRIC = "query-tokens/s and achieved HBM GB/s (% roofline) for C4 top-512 spars
 DEFAULT_WORKLOAD = "c4_decode"
 STORE_METRIC = "KV rows stored/s and achieved HBM GB/s (% roofline) for the FP8 pack-and-store cache write"
 TOPK_METRIC = "query-tokens/s (rows selected) and achieved HBM GB/s (% roofline) for top-k index selection"
+NOMINAL_HBM_GBS = 7900.0      # the part's nominal HBM3e rate, reported beside the measured peak
 
 
 # ---------------------------------------------------------------- helpers
@@ -875,6 +876,7 @@ def run_ours(args):
                 "traffic": ncu_traffic(args.workload), "peak_source": peaks["source"],
                 "algorithmic_bytes_per_launch": nbytes, "flops_per_launch": flops,
                 "hbm_gbs": achieved, "hbm_frac": achieved / peaks["hbm_gbs"],
+                "hbm_frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                 "tensor_tflops": tflops, "tensor_frac": tflops / peaks["bf16_tflops"],
                 "us_per_launch": per_launch_s * 1e6}
     line = {
