@@ -59,7 +59,7 @@ constexpr int kLoadThreads = kLoadWarps * 32;
 constexpr int kQkWarp = kSoftmaxWarps + kLoadWarps;   // S = Q K^T over dims 0..255 (owns the TMEM allocation);
                                                       // warp kQkWarp + 1 takes dims 256..511
 constexpr int kPvWarp = kQkWarp + 2;                  // issues O^T += V^T P^T
-constexpr int kEpiWarp = kPvWarp + 1;                 // idle until the epilogue (one read-out job per warp)
+constexpr int kEpiWarp = kPvWarp + 1;                 // second PV issuer (value tiles 2, 3)
 constexpr int kWarps = kEpiWarp + 1;
 constexpr int kThreads = kWarps * 32;
 static_assert(kWarps == 16, "one O^T read-out job (TMEM quadrant, value tile) per warp");
@@ -334,10 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     const int lane = tid & 31;
     const int G = p.groups;
     const int Sc = p.csplits;
-    const int cs = static_cast<int>(cluster_ctarank());   // slice within the cluster
-    const int grp = blockIdx.x / Sc;                       // head group (one cluster per group)
-    const int t = blockIdx.y;
-    const int gsplit = blockIdx.z;
+    const int cs = static_cast<int>(cluster_ctarank());   // slice within the cluster (= blockIdx.x % Sc)
+    const int grp = (blockIdx.x / Sc) % G;                 // head group (one cluster per group)
+    const int t = blockIdx.x / (Sc * G);                   // query token
+    const int gsplit = blockIdx.y;
     const int split = gsplit * Sc + cs;
     const int head0 = grp * kHG;
     const int hcount = min(kHG, p.H - head0);
@@ -364,16 +364,16 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         mbar_init(bar(B_Q_FULL), kSoftmaxWarps * 32);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(B_KV_FULL + s), kLoadThreads);
-            mbar_init(bar(B_KV_EMPTY + s), 1);
+            mbar_init(bar(B_KV_EMPTY + s), 2);             // both PV issuers
             mbar_init(bar(B_MASK_FULL + s), 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_S_FULL + s), 2);
             mbar_init(bar(B_S_FREE + s), kSoftmaxWarps * 32);
             mbar_init(bar(B_P_FULL + s), kSoftmaxWarps * 32);
-            mbar_init(bar(B_P_FREE + s), 1);
+            mbar_init(bar(B_P_FREE + s), 2);
         }
-        mbar_init(bar(B_O_FINAL), 1);
+        mbar_init(bar(B_O_FINAL), 2);
         mbar_init(bar(B_MERGE), 1);
         fence_mbar_init_cluster();
         *abort_flag = 0;
@@ -581,19 +581,23 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             }
         }
         __syncwarp();
-    } else if (warp == kPvWarp) {
-        // ============================================================ O^T += V^T P^T issuer
+    } else if (warp == kPvWarp || warp == kEpiWarp) {
+        // ============================================================ O^T += V^T P^T issuers
+        // two warps, each over two of the four 128-dim value tiles: a
+        // tcgen05.mma costs its issuing thread about as long as it runs
         if (lane == 0 && ntiles > 0) {
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kHG, true, false);
+            const int mt0 = warp == kPvWarp ? 0 : 2;
             for (int i = 0; i < ntiles; ++i) {
                 const int stage = i % kStages;
                 wait_bar(bar(B_P_FULL + (i & 1)), (i >> 1) & 1, abort_flag);
-                if (i < 8) DSV4_TR(20 + i);
+                if (i < 8 && mt0 == 0) DSV4_TR(20 + i);
                 tc_fence_after();
                 const uint32_t stg = sKV + stage * kStageBytes;
                 const uint32_t pbuf = sP + (i & 1) * kPBytes;
 #pragma unroll
-                for (int mt = 0; mt < 4; ++mt) {
+                for (int m2 = 0; m2 < 2; ++m2) {
+                    const int mt = mt0 + m2;
 #pragma unroll
                     for (int kk = 0; kk < kTileN / 16; ++kk) {
                         // A = V^T (dims 128*mt.., keys 16*kk..): MN-major, 64-dim atoms one chunk apart
@@ -962,9 +966,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
 // L_g * exp(M_g - M) with M the largest of the M_g and the sink; the sink
 // adds exp(sink - M) to the denominator and nothing to the numerator.
 __global__ void __launch_bounds__(256) dsv4_combine_kernel(const __grid_constant__ Params p) {
-    const int t = blockIdx.y;
+    const int nb = (p.H * 64 + 255) / 256;                      // blocks per token
+    const int t = blockIdx.x / nb;
     {
-        const int it = blockIdx.x * blockDim.x + threadIdx.x;   // (head, 8-dim unit)
+        const int it = (blockIdx.x % nb) * blockDim.x + threadIdx.x;   // (head, 8-dim unit)
         if (it >= p.H * 64) return;
         const int h = it >> 6;
         const int u = it & 63;
@@ -1166,7 +1171,6 @@ static int run(const Call& c) {
     if (!c.q || !c.out || !c.seq_lens || !c.sink) return DSV4_ERR_INVALID;
     if (c.T < 1 || c.batch < 1 || c.H < 1 || c.H > 2 * kHG || c.window < 1) return DSV4_ERR_INVALID;
     if (!std::isfinite(c.scale)) return DSV4_ERR_INVALID;
-    if (c.T > 65535) return DSV4_ERR_UNSUPPORTED;
     if (c.ratio != 0 && c.ratio != 4 && c.ratio != 128) return DSV4_ERR_UNSUPPORTED;
     if (reinterpret_cast<uintptr_t>(c.q) % 16 || reinterpret_cast<uintptr_t>(c.out) % 16) return DSV4_ERR_INVALID;
     int rc = check_pool(c.swa);
@@ -1189,7 +1193,7 @@ static int run(const Call& c) {
     make_plan(c.T, G, lmax, c.num_splits, di, sc, sg);
     const int splits = sc * sg;
     const int chunk = (lmax + splits - 1) / splits;   // key slots per slice
-    if (c.T * (long long)sg > 65535) return DSV4_ERR_UNSUPPORTED;
+    if ((long long)c.T * sc * G > 0x7fffffffLL) return DSV4_ERR_UNSUPPORTED;
     const size_t need = workspace_bytes_for(c.T, c.H, sc, sg);
     if (need > 0 && (!c.ws || c.ws_bytes < need)) return DSV4_ERR_WORKSPACE;
 
@@ -1242,7 +1246,7 @@ static int run(const Call& c) {
     cudaStream_t st = static_cast<cudaStream_t>(c.stream);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
-    cfg.gridDim = dim3(sc * G, c.T, sg);
+    cfg.gridDim = dim3(static_cast<unsigned>(sc * G * c.T), sg, 1);   // x: (token, head group, slice)
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemAlloc;
     cfg.stream = st;
@@ -1264,7 +1268,7 @@ static int run(const Call& c) {
         return DSV4_ERR_CUDA;
     }
     if (sg > 1) {
-        dsv4_combine_kernel<<<dim3((c.H * 64 + 255) / 256, c.T), 256, 0, st>>>(p);
+        dsv4_combine_kernel<<<dim3(static_cast<unsigned>((c.H * 64 + 255) / 256 * c.T)), 256, 0, st>>>(p);
         if (cudaGetLastError() != cudaSuccess) return DSV4_ERR_CUDA;
     }
     return DSV4_OK;
@@ -1388,7 +1392,12 @@ int dsv4_attn_c4_sparse_noalloc(const void* q, int32_t batch, int32_t num_heads,
                                 int32_t* debug_rows, void* stream) {
     if (batch < 1 || num_heads < 1 || num_heads > 2 * dsv4::kHG || window < 1 || topk < 1 || num_splits < 0)
         return DSV4_ERR_INVALID;
-    const size_t need = dsv4_attn_workspace_size(batch, num_heads, 4, window, topk, 0, num_splits);
+    // the plan query's own status (a device or argument error) is returned as
+    // is, not mistaken for "needs no scratch"
+    int32_t sc = 1, sg = 1;
+    const int prc = dsv4_attn_plan(batch, num_heads, 4, window, topk, 0, num_splits, &sc, &sg);
+    if (prc != DSV4_OK) return prc;
+    const size_t need = dsv4::workspace_bytes_for(batch, num_heads, sc, sg);
     if (need > DSV4_NOALLOC_SCRATCH_BYTES) return DSV4_ERR_SCRATCH_LIMIT;
     void* scratch = nullptr;
     if (need > 0) {

@@ -176,10 +176,12 @@ int dsv4_attn_verify(const void* q, int32_t num_tokens, int32_t batch, int32_t n
    that cannot allocate device memory themselves: code running where no
    allocator may be called (inside another library's hot loop, in a process
    whose memory is fully reserved up front, or from a runtime that only hands
-   out pointers it owns).  There is no workspace argument: the scratch the
-   split merge needs comes from a buffer inside this library, a static device
-   array of DSV4_NOALLOC_SCRATCH_BYTES that every GPU which loads the library
-   holds until the process exits.  This entry point has no counterpart on the
+   out pointers it owns).  There is no workspace argument: the scratch a
+   split plan needs (the bf16 partial rows the slices of a cluster exchange,
+   and with grid_splits > 1 the fp32 partial results the combine kernel
+   merges) comes from a buffer inside this library, a static device array of
+   DSV4_NOALLOC_SCRATCH_BYTES that every GPU which loads the library holds
+   until the process exits.  This entry point has no counterpart on the
    source pages; it only changes where the scratch lives.
    - The first call on a device looks up the buffer's device address (one
      runtime query, no allocation); make that first call before any stream
@@ -190,7 +192,8 @@ int dsv4_attn_verify(const void* q, int32_t num_tokens, int32_t batch, int32_t n
      writes every scratch byte it later reads.
    - A call whose split plan needs more than DSV4_NOALLOC_SCRATCH_BYTES returns
      DSV4_ERR_SCRATCH_LIMIT and launches nothing (dsv4_attn_workspace_size with
-     the same shapes gives the amount a call needs).
+     the same shapes gives the amount a call needs); a failing plan query
+     returns its own status.
    - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
 #define DSV4_NOALLOC_SCRATCH_BYTES (16u << 20)
 int dsv4_attn_c4_sparse_noalloc(const void* q, int32_t batch, int32_t num_heads,
