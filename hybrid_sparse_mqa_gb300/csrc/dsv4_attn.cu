@@ -52,6 +52,7 @@ constexpr int kTileN = 48;           // keys per tile
 constexpr int kStages = 3;           // gather pipeline depth (48 KB each)
 constexpr int kHG = 64;              // heads per CTA (MMA M of S = Q K^T)
 constexpr int kRingHalf = 192;       // key slots resolved per chunk (four tiles; two chunks held)
+constexpr int kPtCache = 4096;       // extra page-table entries kept for the first chunk (the P area)
 constexpr int kRing = 2 * kRingHalf;
 constexpr int kSoftmaxWarps = 4;
 constexpr int kLoadWarps = 8;
@@ -121,6 +122,7 @@ static_assert(6 * 80 * 128 + 7 * 512 <= kQBytes, "staged peer blocks and (m, l) 
 static_assert(7 * 64 * 128 + 8 * 512 <= kQBytes, "staged peer blocks and (m, l) (Sc = 8) must fit in the Q area");
 static_assert(kMaxCluster * kHG * 4 <= 2 * kPBytes, "merge weights must fit in the P area");
 static_assert(kHG * 4 <= kRing * 4, "single-slice merge weights must fit in the ring");
+static_assert(kPtCache * 4 <= 2 * kPBytes, "first-chunk page-table entries fit in the P area");
 static_assert(kTileN % 16 == 0 && kTileN <= 64, "tile keys: whole K16 steps, one 64-bit mask");
 
 __device__ unsigned int g_dev_error;
@@ -168,7 +170,7 @@ struct Params {
     int topk;
     const float* sink;
     float scale_log2;        // scale * log2(e)
-    int chunk;               // key slots per slice
+    int cw, ce;              // window / extra slots per slice
     int csplits, gsplits;
     __nv_bfloat16* out;
     float* lse;
@@ -179,8 +181,15 @@ struct Params {
     int debug_stride;
 };
 
+// A token's key list is its window slots 0 .. n_swa-1 (positions pos-n_swa+1
+// .. pos) followed by its extra slots 0 .. n_extra-1 (C4 indices or C128
+// compressed-row numbers).  Slice `split` of S takes window slots
+// [w0, w0 + nw) and extra slots [e0, e0 + ne), as equal shares of each part;
+// within the slice its extra slots come first (virtual slots 0 .. ne-1), so
+// the first tiles need only the index list and the extra page table, and the
+// window slots (which need the position first) come last.
 struct TokenInfo {
-    int trow, pos, n_swa, n_c, L, slot_begin, slot_end, ntiles;
+    int trow, pos, n_swa, n_c, n_extra, e0, ne, w0, nw, ntiles;
 };
 
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int* abort_flag) {
@@ -205,7 +214,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int* abo
     return wait_slow(bar, parity, abort_flag);
 }
 
-// Query token t -> request row, position and key-list extent of slice `split`.
+// Query token t -> request row, position and the slots of slice `split`.
 // In decode the request row does not depend on the position, so its load is
 // issued together with the sequence length.
 __device__ void token_info(const Params& p, int t, int split, TokenInfo& ti, unsigned& err) {
@@ -238,61 +247,60 @@ __device__ void token_info(const Params& p, int t, int split, TokenInfo& ti, uns
     ti.trow = trow;
     ti.pos = pos;
     if (!ok) {
-        ti.n_swa = ti.n_c = ti.L = ti.slot_begin = ti.slot_end = ti.ntiles = 0;
+        ti.n_swa = ti.n_c = ti.n_extra = ti.e0 = ti.ne = ti.w0 = ti.nw = ti.ntiles = 0;
         return;
     }
     ti.n_swa = min(pos + 1, p.window);
     ti.n_c = p.ratio ? (pos + 1) / p.ratio : 0;
-    const int n_extra = p.ratio == 4 ? p.topk : (p.ratio == 128 ? ti.n_c : 0);
-    ti.L = ti.n_swa + n_extra;
-    if (ti.L > p.chunk * p.csplits * p.gsplits) err |= DSV4_DEV_ERR_PLAN;
-    ti.slot_begin = split * p.chunk;
-    ti.slot_end = min(ti.slot_begin + p.chunk, ti.L);
-    ti.ntiles = ti.slot_end > ti.slot_begin ? (ti.slot_end - ti.slot_begin + kTileN - 1) / kTileN : 0;
+    ti.n_extra = p.ratio == 4 ? p.topk : (p.ratio == 128 ? ti.n_c : 0);
+    const int S = p.csplits * p.gsplits;
+    if (ti.n_swa > p.cw * S || ti.n_extra > p.ce * S) err |= DSV4_DEV_ERR_PLAN;
+    ti.e0 = min(split * p.ce, ti.n_extra);
+    ti.ne = min(ti.e0 + p.ce, ti.n_extra) - ti.e0;
+    ti.w0 = min(split * p.cw, ti.n_swa);
+    ti.nw = min(ti.w0 + p.cw, ti.n_swa) - ti.w0;
+    ti.ntiles = (ti.ne + ti.nw + kTileN - 1) / kTileN;
 }
 
-// C4 index of key slot `slot` (extra slots only).  With `has_spec`, `spec`
-// holds the index loaded for slot - window before the position was known,
-// which is the right one whenever the whole window is present.
-__device__ __forceinline__ int c4_index(const Params& p, int t, const TokenInfo& ti, int slot, bool has_spec,
-                                        int spec) {
-    return has_spec && ti.n_swa == p.window ? spec : __ldg(p.topk_idx + (size_t)t * p.topk + (slot - ti.n_swa));
+// Window slot w -> physical SWA pool row (-1 = skipped).
+__device__ __forceinline__ int resolve_window(const Params& p, const TokenInfo& ti, int w, unsigned& err) {
+    const int j = ti.pos - ti.n_swa + 1 + w;
+    const int lp = j / kPageSize;
+    if (lp >= p.swa_pt_stride) { err |= DSV4_DEV_ERR_SWA_PAGE; return -1; }
+    const int page = __ldg(p.swa_pt + (size_t)ti.trow * p.swa_pt_stride + lp);
+    if (page < 0 || page >= p.swa_pages) { err |= DSV4_DEV_ERR_SWA_PAGE; return -1; }
+    return page * kPageSize + (j % kPageSize);
 }
 
-// Key slot -> physical pool row (-1 = skipped).  Window slots are positions
-// pos-n_swa+1 .. pos in the SWA pool; extra slots are C4 indices or C128
-// compressed-row numbers in the extra pool.  `idx` is the slot's C4 index.
-__device__ __forceinline__ int resolve_slot_idx(const Params& p, const TokenInfo& ti, int slot, int idx,
-                                                unsigned& err) {
-    if (slot < ti.n_swa) {
-        const int j = ti.pos - ti.n_swa + 1 + slot;
-        const int lp = j / kPageSize;
-        if (lp >= p.swa_pt_stride) { err |= DSV4_DEV_ERR_SWA_PAGE; return -1; }
-        const int page = __ldg(p.swa_pt + (size_t)ti.trow * p.swa_pt_stride + lp);
-        if (page < 0 || page >= p.swa_pages) { err |= DSV4_DEV_ERR_SWA_PAGE; return -1; }
-        return page * kPageSize + (j % kPageSize);
-    }
+// Extra slot with C4 index (or C128 compressed-row number) idx -> physical
+// extra pool row (-1 = skipped).  `cache` (nullable) holds the request's
+// extra page-table entries for logical pages lp_lo .. lp_lo + ncache - 1.
+__device__ __forceinline__ int resolve_extra(const Params& p, const TokenInfo& ti, int idx, const int* cache,
+                                             int lp_lo, int ncache, unsigned& err) {
     if (p.ratio == 4) {
         if (idx < 0) return -1;
         if (idx >= ti.n_c) { err |= DSV4_DEV_ERR_INDEX_RANGE; return -1; }
-    } else {
-        idx = slot - ti.n_swa;
     }
     const int lp = idx / kPageSize;
     if (lp >= p.ex_pt_stride) { err |= DSV4_DEV_ERR_EXTRA_PAGE; return -1; }
-    const int page = __ldg(p.ex_pt + (size_t)ti.trow * p.ex_pt_stride + lp);
+    const int page = (cache != nullptr && lp >= lp_lo && lp < lp_lo + ncache)
+                         ? cache[lp - lp_lo]
+                         : __ldg(p.ex_pt + (size_t)ti.trow * p.ex_pt_stride + lp);
     if (page < 0 || page >= p.ex_pages) { err |= DSV4_DEV_ERR_EXTRA_PAGE; return -1; }
     return page * kPageSize + (idx % kPageSize);
 }
 
-__device__ __forceinline__ int resolve_slot(const Params& p, int t, const TokenInfo& ti, int slot, unsigned& err) {
-    const int idx = (p.ratio == 4 && slot >= ti.n_swa) ? __ldg(p.topk_idx + (size_t)t * p.topk + (slot - ti.n_swa)) : 0;
-    return resolve_slot_idx(p, ti, slot, idx, err);
+// Key slot (position in the token's list) -> physical row, for the debug dump.
+__device__ __forceinline__ int resolve_key_slot(const Params& p, int t, const TokenInfo& ti, int slot, unsigned& err) {
+    if (slot < ti.n_swa) return resolve_window(p, ti, slot, err);
+    const int e = slot - ti.n_swa;
+    const int idx = p.ratio == 4 ? __ldg(p.topk_idx + (size_t)t * p.topk + e) : e;
+    return resolve_extra(p, ti, idx, nullptr, 0, 0, err);
 }
 
-__device__ __forceinline__ const uint8_t* slot_row_ptr(const Params& p, const TokenInfo& ti, int slot, int row) {
-    return slot < ti.n_swa ? p.swa_rows + (size_t)row * p.swa_row_bytes
-                           : p.ex_rows + (size_t)row * p.ex_row_bytes;
+// Source row of the slice's virtual slot v (extra slots first) in its pool.
+__device__ __forceinline__ const uint8_t* slot_row_ptr(const Params& p, const TokenInfo& ti, int v, int row) {
+    return v < ti.ne ? p.ex_rows + (size_t)row * p.ex_row_bytes : p.swa_rows + (size_t)row * p.swa_row_bytes;
 }
 
 // Byte offset of 16-byte piece `piece` (0..7) of the 128-byte line `line` in
@@ -387,18 +395,30 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     if (warp < 4 && lane < 16 && 16 * warp + lane < hcount) sink_l2 = __ldg(p.sink + head0 + 16 * warp + lane) * kLog2e;
 
     // ------------------------------------------------------------ set-up
-    // C4: each loader thread fetches the index of its first-chunk slot before
-    // the token's position is known, assuming the whole window is present
-    // (key list window + topk long; the slot layout is the one below)
-    int idx_spec = -1;
-    if (is_loader && p.ratio == 4 && lt < kRingHalf) {
-        const int b0 = split * p.chunk, e0 = min(b0 + p.chunk, p.window + p.topk);
-        if (e0 > b0) {
-            const int nt = (e0 - b0 + kTileN - 1) / kTileN;
-            const int sl = b0 + lt - (nt * kTileN - (e0 - b0));
-            const int e = sl - p.window;
-            if (sl >= b0 && e >= 0 && e < p.topk) idx_spec = __ldg(p.topk_idx + (size_t)t * p.topk + e);
-        }
+    // Loads that need no position, issued together with the position's: the
+    // C4 index of this loader thread's first extra slot, and (when the
+    // request row is the token's own) the slice's entries of the extra page
+    // table, kept for the first 192 slots in the P area (free until the first
+    // probabilities).  C4 indices can point anywhere in the request, so C4
+    // keeps the row's first kPtCache entries; a C128 slice reads its own
+    // contiguous range.
+    int* pt_cache = reinterpret_cast<int*>(smem + OFF_P);
+    const int e0n = split * p.ce;                        // the slice's first extra slot
+    int lp_lo = 0, ncache = 0;
+    if (p.ratio == 4) {
+        ncache = min(p.ex_pt_stride, kPtCache);
+    } else if (p.ratio == 128) {
+        lp_lo = e0n / kPageSize;
+        ncache = max(0, min(p.ex_pt_stride - lp_lo, (min(p.ce, kRingHalf) + kPageSize - 1) / kPageSize + 1));
+    }
+    const bool early_row = p.cu_seqlens == nullptr && p.rpi == nullptr && p.ratio != 0 && t < p.ex_pt_rows;
+    int pre_idx = -1;
+    if (is_loader) {
+        if (p.ratio == 4 && lt < min(p.ce, kRingHalf) && e0n + lt < p.topk)
+            pre_idx = __ldg(p.topk_idx + (size_t)t * p.topk + e0n + lt);
+        if (early_row)
+            for (int k = lt; k < ncache; k += kLoadThreads)
+                pt_cache[k] = __ldg(p.ex_pt + (size_t)t * p.ex_pt_stride + lp_lo + k);
     }
     // every thread derives the token's coordinates itself (same addresses; the
     // loads overlap the barrier set-up); thread 0 reports the errors
@@ -408,6 +428,12 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         token_info(p, t, split, ti, e0);
         if (tid == 0) err |= e0;
     }
+    if (is_loader && !early_row && p.ratio != 0 && ti.ntiles > 0)
+        for (int k = lt; k < ncache; k += kLoadThreads)
+            pt_cache[k] = __ldg(p.ex_pt + (size_t)ti.trow * p.ex_pt_stride + lp_lo + k);
+    // the early C4 indices by extra slot (the thread that resolves slot e0 + v
+    // depends on the padding, known only now), in ring half 1 until chunk 1
+    if (is_loader && lt < kRingHalf) ring[kRingHalf + lt] = pre_idx;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -419,28 +445,49 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         // ============================================================ loader
         const int lw = lt >> 5;
         if (p.debug_rows != nullptr && grp == 0) {
-            const int d0 = split * p.chunk;
-            const int d1 = min(d0 + p.chunk, p.debug_stride);
-            for (int s = d0 + lt; s < d1; s += kLoadThreads) {
-                const int row = (s < ti.L) ? resolve_slot(p, t, ti, s, err) : -1;
-                p.debug_rows[(size_t)t * p.debug_stride + s] = row;
-            }
+            // this slice's key slots (slice 0 also marks the unused tail)
+            int* dbg = p.debug_rows + (size_t)t * p.debug_stride;
+            for (int w = lt; w < ti.nw; w += kLoadThreads)
+                dbg[ti.w0 + w] = resolve_window(p, ti, ti.w0 + w, err);
+            for (int e = lt; e < ti.ne; e += kLoadThreads)
+                dbg[ti.n_swa + ti.e0 + e] = resolve_key_slot(p, t, ti, ti.n_swa + ti.e0 + e, err);
+            if (split == 0)
+                for (int k = ti.n_swa + ti.n_extra + lt; k < p.debug_stride; k += kLoadThreads) dbg[k] = -1;
         }
-        const int nslots = ti.slot_end - ti.slot_begin;
-        // Tile i holds the virtual slots 48 i .. 48 i + 47; virtual slot v is
-        // key slot slot_begin + v - shift, and v < shift are padding.  The short
-        // tile of a slice is its first one: it finishes early and frees a stage
-        // while the full tiles are still landing.
-        const int shift = ntiles * kTileN - nslots;
-        // chunk c of the slice (kRingHalf virtual slots) goes to ring half c & 1
+        const int nv = ti.ne + ti.nw;                    // the slice's slots
+        // Tile i holds the tile positions 48 i .. 48 i + 47; position u is the
+        // slice's virtual slot u - shift (extra slots first, then window
+        // slots), and u < shift are padding.  The short tile of a slice is its
+        // first one: it finishes early and frees a stage while the full tiles
+        // are still landing.
+        const int shift = ntiles * kTileN - nv;
+        // Chunk c of the slice (kRingHalf positions) goes to ring half c & 1.
+        // In chunk 0 the extra slots resolve from the loads issued with the
+        // position; a window slot's page-table load is issued then too, and
+        // its row is entered only before the first tile that holds a window
+        // slot, so the extra-only tiles start one round trip earlier.
+        const int u_win = ti.ne + shift;                 // tile position of the first window slot
+        const int win_tile = (u_win < kRingHalf && ti.nw > 0) ? u_win / kTileN : -1;   // in chunk 0
+        int win_j = -1, win_page = -1;                   // a deferred window slot: position, raw page id
         auto resolve_chunk = [&](int c) {
             if (lt >= kRingHalf) return;
-            const int v = c * kRingHalf + lt;
-            const int sl = ti.slot_begin + v - shift;
+            const int v = c * kRingHalf + lt - shift;
             int row = -1;
-            if (v >= shift && sl < ti.slot_end) {
-                const int idx = (p.ratio == 4 && sl >= ti.n_swa) ? c4_index(p, t, ti, sl, c == 0, idx_spec) : 0;
-                row = resolve_slot_idx(p, ti, sl, idx, err);
+            if (v >= 0 && v < nv) {
+                if (v < ti.ne) {
+                    const int e = ti.e0 + v;
+                    const int idx = p.ratio == 4 ? (c == 0 ? ring[kRingHalf + v] : __ldg(p.topk_idx + (size_t)t * p.topk + e)) : e;
+                    row = resolve_extra(p, ti, idx, pt_cache, lp_lo, c == 0 ? ncache : 0, err);
+                } else if (c == 0 && win_tile >= 0) {
+                    // only issue the page-table load here; its value is used
+                    // before tile win_tile, so this thread does not wait on it now
+                    win_j = ti.pos - ti.n_swa + 1 + ti.w0 + v - ti.ne;
+                    const int lp = win_j / kPageSize;
+                    if (lp < p.swa_pt_stride) win_page = __ldg(p.swa_pt + (size_t)ti.trow * p.swa_pt_stride + lp);
+                    else win_j = -2;
+                } else {
+                    row = resolve_window(p, ti, ti.w0 + v - ti.ne, err);
+                }
             }
             ring[(c & 1) * kRingHalf + lt] = row;
         };
@@ -454,7 +501,18 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             const int stage = i % kStages, use = i / kStages;
             const int c = i >> 2;
             if ((i & 3) == 0 && i > 0) named_barrier_sync(1, kLoadThreads);   // chunk c resolved
-            const int slot0 = ti.slot_begin + i * kTileN - shift;           // key slot of row 0 (may be padding)
+            if (i == win_tile) {
+                // chunk 0's window slots
+                const int v = lt - shift;
+                if (lt < kRingHalf && v >= ti.ne && v < nv) {
+                    int row = -1;
+                    if (win_j == -2 || win_page < 0 || win_page >= p.swa_pages) err |= DSV4_DEV_ERR_SWA_PAGE;
+                    else row = win_page * kPageSize + (win_j % kPageSize);
+                    ring[lt] = row;
+                }
+                named_barrier_sync(1, kLoadThreads);
+            }
+            const int v0 = i * kTileN - shift;                                // virtual slot of row 0 (may be padding)
             const int* rg = ring + (c & 1) * kRingHalf + (i & 3) * kTileN;   // this tile's rows
             const uint32_t dst_stage = sKV + stage * kStageBytes;
             if constexpr (KV_FORMAT == DSV4_KV_BF16) {
@@ -465,9 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
 #pragma unroll
                 for (int k = 0; k < kR; ++k) {
                     const int r = lw * kR + k;
-                    const int slot = slot0 + r;
-                    const int row = (slot >= ti.slot_begin && slot < ti.slot_end) ? rg[r] : -1;
-                    const uint8_t* src = row >= 0 ? slot_row_ptr(p, ti, slot, row) : p.swa_rows;
+                    const int v = v0 + r;
+                    const int row = (v >= 0 && v < nv) ? rg[r] : -1;
+                    const uint8_t* src = row >= 0 ? slot_row_ptr(p, ti, v, row) : p.swa_rows;
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         const int piece = lane + 32 * h2;       // 16-byte piece of the 1 KB row
@@ -486,12 +544,12 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
 #pragma unroll
                 for (int k = 0; k < kR; ++k) {
                     const int r = lw * kR + k;
-                    const int slot = slot0 + r;
-                    const int row = (slot >= ti.slot_begin && slot < ti.slot_end) ? rg[r] : -1;
+                    const int v = v0 + r;
+                    const int row = (v >= 0 && v < nv) ? rg[r] : -1;
                     raw[k] = raw2[k] = make_uint4(0, 0, 0, 0);
                     scl[k] = 0.f;
                     if (row >= 0) {
-                        const uint8_t* src = slot_row_ptr(p, ti, slot, row);
+                        const uint8_t* src = slot_row_ptr(p, ti, v, row);
                         if (lane < 28) {
                             raw[k] = __ldg(reinterpret_cast<const uint4*>(src + lane * 16));
                             scl[k] = __ldg(reinterpret_cast<const float*>(src + kFp8ScaleOff) + (lane >> 2));
@@ -534,11 +592,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             }
             if (lw == 0) {
                 // validity of the tile's key slots (lane l: rows l and 32 + l)
-                const bool v0 = slot0 + lane >= ti.slot_begin && slot0 + lane < ti.slot_end && rg[lane] >= 0;
-                const bool v1 = lane + 32 < kTileN && slot0 + lane + 32 >= ti.slot_begin &&
-                                slot0 + lane + 32 < ti.slot_end && rg[lane + 32] >= 0;
-                const unsigned b0 = __ballot_sync(0xffffffffu, v0);
-                const unsigned b1 = __ballot_sync(0xffffffffu, v1);
+                const bool ok0 = v0 + lane >= 0 && v0 + lane < nv && rg[lane] >= 0;
+                const bool ok1 = lane + 32 < kTileN && v0 + lane + 32 >= 0 && v0 + lane + 32 < nv && rg[lane + 32] >= 0;
+                const unsigned b0 = __ballot_sync(0xffffffffu, ok0);
+                const unsigned b1 = __ballot_sync(0xffffffffu, ok1);
                 if (lane == 0) {
                     *reinterpret_cast<volatile uint64_t*>(smem + OFF_MASK + stage * 8) =
                         static_cast<uint64_t>(b0) | (static_cast<uint64_t>(b1) << 32);
@@ -548,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             if (lt == 0 && i < 8) DSV4_TR(4 + i);
             // resolve the next chunk once this one's first two tiles are on their way
             // (ring half (c + 1) & 1 was last read by chunk c - 1, finished by all)
-            if ((i & 3) == 1 && (c + 1) * kRingHalf < nslots) resolve_chunk(c + 1);
+            if ((i & 3) == 1 && (c + 1) * kRingHalf < nv + shift) resolve_chunk(c + 1);
         }
         cp_async_wait_all();
     } else if (warp == kQkWarp || warp == kQkWarp + 1) {
@@ -1192,7 +1249,8 @@ static int run(const Call& c) {
     int sc = 1, sg = 1;
     make_plan(c.T, G, lmax, c.num_splits, di, sc, sg);
     const int splits = sc * sg;
-    const int chunk = (lmax + splits - 1) / splits;   // key slots per slice
+    // each slice takes an equal share of the window slots and of the extra slots
+    const int cw = (c.window + splits - 1) / splits, ce = (lmax - c.window + splits - 1) / splits;
     if ((long long)c.T * sc * G > 0x7fffffffLL) return DSV4_ERR_UNSUPPORTED;
     const size_t need = workspace_bytes_for(c.T, c.H, sc, sg);
     if (need > 0 && (!c.ws || c.ws_bytes < need)) return DSV4_ERR_WORKSPACE;
@@ -1227,7 +1285,8 @@ static int run(const Call& c) {
     p.topk = c.topk;
     p.sink = c.sink;
     p.scale_log2 = static_cast<float>(static_cast<double>(c.scale) * 1.4426950408889634);
-    p.chunk = chunk;
+    p.cw = cw;
+    p.ce = ce;
     p.csplits = sc;
     p.gsplits = sg;
     p.out = static_cast<__nv_bfloat16*>(c.out);
