@@ -116,6 +116,71 @@ def ncu_traffic(workload):
     return ent.get("dram_bytes_per_launch")
 
 
+# ---------------------------------------------------------------- oracle timing
+_ORACLE = {}
+
+
+def _oracle_init(inp):
+    """Pool worker set-up: the inputs arrive as shared CPU tensors (BLAS runs
+    one thread per process: the spawning parent set that in the environment
+    the worker inherits)."""
+    sys.path.insert(0, ROOT)
+    from oracle import dsv4_oracle as O
+    _ORACLE["O"] = O
+    _ORACLE["kw"] = inp.oracle_kwargs()
+    O.dsv4_attention(**_ORACLE["kw"], tokens=[0])
+
+
+def _oracle_tokens(tokens):
+    _ORACLE["O"].dsv4_attention(**_ORACLE["kw"], tokens=list(tokens))
+    return len(tokens)
+
+
+def oracle_pool(inp_cpu, workers):
+    """A pool of `workers` spawned processes, each holding the workload's
+    inputs (shared CPU tensors) and running the oracle with one BLAS thread."""
+    import multiprocessing as mp
+    import torch  # noqa: F401  (registers the shared-memory pickling of CPU tensors)
+    for name in ("q", "seq_lens", "swa_pool", "swa_page_table", "extra_pool", "extra_page_table", "topk_idx",
+                 "sink", "cu_seqlens_q", "req_pool_indices"):
+        x = getattr(inp_cpu, name, None)
+        if x is not None:
+            x.share_memory_()
+    saved = {v: os.environ.get(v) for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for v in saved:
+        os.environ[v] = "1"
+    try:
+        pool = mp.get_context("spawn").Pool(workers, initializer=_oracle_init, initargs=(inp_cpu,))
+    finally:
+        for v, old in saved.items():
+            if old is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = old
+    pool.map(_oracle_tokens, [[0]] * workers, chunksize=1)      # every worker is up
+    return pool
+
+
+def oracle_throughput(inp_cpu, workers, seconds, per_task=4):
+    """Query tokens per second of the float64 oracle on this host: `workers`
+    processes (one BLAS thread each), tasks of `per_task` consecutive tokens,
+    best of three runs of about `seconds` each."""
+    T = inp_cpu.T
+    with oracle_pool(inp_cpu, workers) as pool:
+        probe = [[(k * per_task + i) % T for i in range(per_task)] for k in range(workers)]
+        t0 = time.perf_counter()
+        pool.map(_oracle_tokens, probe, chunksize=1)
+        per_round = max(time.perf_counter() - t0, 1e-4)
+        rounds = max(1, int(seconds / per_round))
+        tasks = [[(k * per_task + i) % T for i in range(per_task)] for k in range(rounds * workers)]
+        best = 0.0
+        for _ in range(3):
+            t0 = time.perf_counter()
+            done = sum(pool.map(_oracle_tokens, tasks, chunksize=1))
+            best = max(best, done / (time.perf_counter() - t0))
+    return best, rounds * workers * per_task
+
+
 def hold_stream(stream, cycles=2_000_000):
     """Keep the launch stream busy for a fixed number of GPU cycles (about
     1 ms; the spin reads nothing and waits on nothing) so that the host has
@@ -291,8 +356,9 @@ def run_reference_store(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "rows_per_step": per,
                    "note": f"oracle sample: {per} of the {n} new rows per step"},
-        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"{args.steps} steps x {per} rows of {args.workload}"},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} steps x {per} rows of {args.workload}, one process "
+                                   f"(the oracle's numpy code runs on one core)"},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -323,7 +389,7 @@ def run_reference_topk(args):
         "vs_baseline": None, "dtype": "u32", "data": "synthetic",
         "config": {"workload": args.workload, "rows_per_step": per,
                    "note": f"oracle sample: one of the {rows} rows per step"},
-        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": os.cpu_count(), "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} rows of {args.workload}, one per step"},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -332,30 +398,29 @@ def run_reference_topk(args):
 
 
 def run_reference(args):
-    import numpy as np
-    import torch
+    """The oracle as it stands (numpy float64) on the host's cores: every step
+    is a bounded sample of the workload's query tokens spread over one
+    spawned process per core (one BLAS thread each)."""
     from hybrid_sparse_mqa_gb300 import synth
-    from oracle import dsv4_oracle as O
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     inp = synth.make_inputs(args.workload, device="cpu")
-    kw = inp.oracle_kwargs()
     T = inp.T
-    per_step_tokens = min(T, args.ref_tokens)
-    # one warm-up token, then W + K bounded steps over `per_step_tokens` tokens each
-    O.dsv4_attention(**kw, tokens=[0])
-    for w in range(args.warmup):
-        O.dsv4_attention(**kw, tokens=list(range(min(per_step_tokens, T))))
-    t0 = time.perf_counter()
-    done = 0
-    for k in range(args.steps):
-        toks = [(k * per_step_tokens + i) % T for i in range(per_step_tokens)]
-        O.dsv4_attention(**kw, tokens=toks)
-        done += len(toks)
-    dt = time.perf_counter() - t0
+    cores = os.cpu_count() or 1
+    per_step_tokens = min(T, max(args.ref_tokens, cores))
+    with oracle_pool(inp, cores) as pool:
+        def step(k):
+            toks = [[(k * per_step_tokens + i) % T] for i in range(per_step_tokens)]
+            return sum(pool.map(_oracle_tokens, toks, chunksize=1))
+        for w in range(args.warmup):
+            step(w)
+        t0 = time.perf_counter()
+        done = 0
+        for k in range(args.steps):
+            done += step(k)
+        dt = time.perf_counter() - t0
     value = done / dt
-    cores = os.cpu_count()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "query-tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -364,7 +429,8 @@ def run_reference(args):
         "config": {"workload": args.workload, "tokens_per_step": per_step_tokens,
                    "note": f"oracle sample: {per_step_tokens} of the {T} query tokens per step"},
         "cpu_baseline": {"value": value, "unit": "query-tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{args.steps} steps x {per_step_tokens} tokens of {args.workload}"},
+                         "sample": f"{args.steps} steps x {per_step_tokens} tokens of {args.workload}, "
+                                   f"{cores} spawned processes with one BLAS thread each"},
         "e2e": {"value": value, "unit": "query-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -505,7 +571,7 @@ def run_store(args):
             O.kv_store(**sub)
             done += per
         dt = time.perf_counter() - t0
-        cpu_baseline = {"value": done / dt, "unit": "rows/s", "cores": os.cpu_count(), "kind": "oracle",
+        cpu_baseline = {"value": done / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
                         "sample": f"{done // per} oracle calls of {per} rows of {args.workload}, {dt:.1f} s, "
                                   f"numpy (pack vectorised, placement one row at a time)"}
 
@@ -721,6 +787,90 @@ def run_topk(args):
 
 
 # ---------------------------------------------------------------- our arm
+SECOND_WORKLOAD = "c128_decode"     # the other decode configuration with a roofline target
+
+
+def measure_workload(args, workload, dev, world, steps):
+    """Times `steps` calls of `workload` exactly as the headline line does
+    (rotating input sets with their own pools, CUDA-graph replays on a busy
+    stream, CUDA events on the launch stream, slowest rank) and returns its
+    entry: throughput and the roofline of one call."""
+    import torch
+    from hybrid_sparse_mqa_gb300 import attn, synth
+    rank, _, _ = dist_env()
+    sets = [synth.make_inputs(workload, device=dev, seed=2000 * (rank + 1) + r) for r in range(args.sets)]
+    inp0 = sets[0]
+    T, H = inp0.T, inp0.H
+    w = inp0.work
+    nbytes, flops = algorithmic_bytes_and_flops(inp0)
+    outs = [torch.empty_like(x.q) for x in sets]
+    lses = [torch.empty(T, H, dtype=torch.float32, device=dev) for _ in sets]
+    topk = w.topk if w.ratio == 4 else 0
+    sc, sg = attn.dsv4_attn_plan(T, H, w.ratio, w.window, topk, inp0.max_seq_len, 0)
+    wsz = attn.dsv4_attn_workspace_size(T, H, w.ratio, w.window, topk, inp0.max_seq_len, 0)
+    ws = torch.empty(max(wsz, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(k, st):
+        i = k % len(sets)
+        attn.run_inputs(sets[i], out=outs[i], lse=lses[i], workspace=ws, stream=st)
+
+    with torch.cuda.stream(stream):
+        for k in range(max(args.warmup, 1)):
+            step(k, stream)
+    torch.cuda.synchronize()
+    R = len(sets)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for k in range(R):
+            step(k, torch.cuda.current_stream())
+    full, rem = divmod(steps, R)
+    tail = None
+    if rem:
+        tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tail, stream=stream):
+            for k in range(rem):
+                step(k, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hold_stream(stream)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(full):
+            graph.replay()
+        if tail is not None:
+            tail.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = slowest_ms(ev0.elapsed_time(ev1), world, dev)
+    flags = attn.dsv4_attn_get_device_error(stream)
+    sec = ms / 1e3 / steps
+    peaks = measured_peaks()
+    achieved = nbytes / sec / 1e9
+    tflops = flops / sec / 1e12
+    tensor_bound = flops / (peaks["bf16_tflops"] * 1e12) > nbytes / (peaks["hbm_gbs"] * 1e9)
+    return {
+        "value": job_tokens_per_s(T, world, sec), "unit": "query-tokens/s", "ms_per_step": sec * 1e3,
+        "steps": steps, "device_error_flags": flags,
+        "config": {"workload": workload, "batch": w.batch, "heads": H, "context": int(inp0.max_seq_len),
+                   "split_plan": {"cluster_splits": sc, "grid_splits": sg}, "input_sets": R},
+        "gpu_launches": steps * (2 if sg > 1 else 1),
+        "roofline": {"bound": "tensor" if tensor_bound else "hbm",
+                     "achieved": tflops if tensor_bound else achieved,
+                     "peak": peaks["bf16_tflops"] if tensor_bound else peaks["hbm_gbs"],
+                     "unit": "TFLOP/s" if tensor_bound else "GB/s",
+                     "frac": tflops / peaks["bf16_tflops"] if tensor_bound else achieved / peaks["hbm_gbs"],
+                     "traffic": ncu_traffic(workload), "peak_source": peaks["source"],
+                     "algorithmic_bytes_per_launch": nbytes, "flops_per_launch": flops,
+                     "hbm_gbs": achieved, "hbm_frac": achieved / peaks["hbm_gbs"],
+                     "tensor_tflops": tflops, "tensor_frac": tflops / peaks["bf16_tflops"],
+                     "us_per_launch": sec * 1e6},
+    }
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -856,21 +1006,23 @@ def run_ours(args):
     ems = slowest_ms(e0.elapsed_time(e1), world, dev)
     e2e_value = job_tokens_per_s(T, world, ems / 1e3 / e2e_steps)
 
+    # ---- the other decode configuration with a roofline target, timed the same way
+    second = None
+    if args.workload == DEFAULT_WORKLOAD and args.num_splits == 0 and not args.no_second:
+        second = measure_workload(args, SECOND_WORKLOAD, dev, world, args.steps)
+
     # ---- oracle on the host, bounded sample of the same workload (rank 0, N=1)
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
-        from oracle import dsv4_oracle as O
-        kw = sets[0].oracle_kwargs()
-        O.dsv4_attention(**kw, tokens=[0])
-        t0 = time.perf_counter()
-        n = 0
-        while time.perf_counter() - t0 < args.cpu_seconds and n < T * 10000:
-            O.dsv4_attention(**kw, tokens=[n % T])
-            n += 1
-        dt = time.perf_counter() - t0
-        cpu_baseline = {"value": n / dt, "unit": "query-tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                        "sample": f"{n} query tokens of {args.workload} one at a time, {dt:.1f} s, numpy "
-                                  f"float64 (BLAS threads = host default)"}
+        inp_cpu = synth.make_inputs(args.workload, device="cpu", seed=1000 * (rank + 1))
+        cores = os.cpu_count() or 1
+        v_all, n_all = oracle_throughput(inp_cpu, cores, args.cpu_seconds / 6)
+        v_one, n_one = oracle_throughput(inp_cpu, 1, args.cpu_seconds / 6)
+        cpu_baseline = {"value": v_all, "unit": "query-tokens/s", "cores": cores, "kind": "oracle",
+                        "one_core": v_one,
+                        "sample": f"{args.workload} query tokens, numpy float64, tasks of 4 tokens: {cores} spawned "
+                                  f"processes with one BLAS thread each ({n_all} tokens per run) and 1 process "
+                                  f"({n_one} tokens per run), best of 3 runs each"}
 
     if rank != 0:
         if world > 1:
@@ -922,6 +1074,8 @@ def run_ours(args):
         "clocks": clocks.summary(),
         "device_error_flags": flags,
     }
+    if second is not None:
+        line[SECOND_WORKLOAD] = second
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
@@ -944,6 +1098,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4096,
                     help="rows per oracle call for the cache-write workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-second", action="store_true",
+                    help=f"skip the {SECOND_WORKLOAD} entry of the default line")
     ap.add_argument("--quick", action="store_true",
                     help="no clock sampling, no CPU baseline (for profiler runs)")
     args = ap.parse_args()

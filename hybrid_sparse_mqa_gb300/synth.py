@@ -79,6 +79,9 @@ PRESETS = {
     # sparse prefill / extend: 4 requests each appending a 1024-token chunk at
     # the end of a 65536-token context, C4 top-512 per query token
     "c4_prefill": Workload("c4_prefill", batch=4, heads=64, ratio=4, seq_lens=(65536,) * 4, qlen=1024, seed=5),
+    # small batch x long compressed list: C128 decode of 2 requests at 1M
+    # context, whose split plan merges cluster groups with the combine kernel
+    "c128_decode_b2": Workload("c128_decode_b2", batch=2, heads=128, ratio=128, seq_lens=(1048576,) * 2, seed=6),
 }
 
 
@@ -239,7 +242,10 @@ def make_inputs(work: Workload | str, device="cpu", seed=None, **overrides) -> I
         extra_table, extra_pages = _page_tables(needed, num_req_rows, width, work.decoy_pages, gen_cpu)
         extra_pool = _pool(extra_pages * PAGE, work.kv_format, gen_dev, dev)
     if work.ratio == 4:
-        topk = _topk_lists(seq, qlen, work.topk, gen_cpu)
+        # the workloads hold valid index lists: a query token at position p
+        # draws from the compressed rows of its complete groups of 4 positions
+        visible = [(s_ - qlen + i + 1) // 4 for s_ in seq for i in range(qlen)]
+        topk = _topk_lists(visible, work.topk, gen_cpu)
 
     q = _randn_bf16((T, H, DIM), gen_dev, dev)
     sink = torch.randn(H, generator=gen_cpu).float()
@@ -390,22 +396,20 @@ def make_topk_inputs(work: TopkWorkload | str, device="cpu", seed=None) -> TopkI
     return TopkInputs(work=work, scores=scores, lengths=torch.tensor(lengths, dtype=torch.int32, device=dev))
 
 
-def _topk_lists(seq, qlen, topk, gen_cpu):
-    """Per query token: min(topk, n_c) distinct uniform indices in [0, n_c(p)),
-    unsorted, padded with -1 (n_c(p) = (p+1)//4 compressed rows are visible)."""
+def _topk_lists(visible, topk, gen_cpu):
+    """Per query token: min(topk, n) distinct uniform indices in [0, n),
+    unsorted, padded with -1, where n is that token's entry of `visible`
+    (the number of compressed rows it may index, given by the caller)."""
     rows = []
-    for s in seq:
-        for i in range(qlen):
-            p = s - qlen + i
-            n_c = (p + 1) // 4
-            k = min(topk, n_c)
-            if n_c <= 4 * topk:
-                pick = torch.randperm(n_c, generator=gen_cpu)[:k]
-            else:
-                # rejection-free distinct draw: random keys, keep the k largest
-                pick = torch.rand(n_c, generator=gen_cpu).topk(k).indices
-                pick = pick[torch.randperm(k, generator=gen_cpu)]
-            row = torch.full((topk,), -1, dtype=torch.int32)
-            row[:k] = pick.to(torch.int32)
-            rows.append(row)
+    for n_c in visible:
+        k = min(topk, n_c)
+        if n_c <= 4 * topk:
+            pick = torch.randperm(n_c, generator=gen_cpu)[:k]
+        else:
+            # rejection-free distinct draw: random keys, keep the k largest
+            pick = torch.rand(n_c, generator=gen_cpu).topk(k).indices
+            pick = pick[torch.randperm(k, generator=gen_cpu)]
+        row = torch.full((topk,), -1, dtype=torch.int32)
+        row[:k] = pick.to(torch.int32)
+        rows.append(row)
     return torch.stack(rows) if rows else torch.zeros((0, topk), dtype=torch.int32)

@@ -170,14 +170,33 @@ def test_device_errors_are_flagged_not_trapped(attn):
 
 # ---------------------------------------------------------------- full-size workloads
 @pytest.mark.parametrize("name,tokens", [
-    ("swa_decode", [0, 17, 40, 63]),
-    ("c4_decode", [0, 9, 31]),
-    ("c128_decode", [0, 15]),
-    ("c4_prefill", [0, 511, 1023, 1024, 2900, 4095]),
+    ("swa_decode", None),                        # every token
+    ("c4_decode", None),
+    ("c128_decode", None),
+    ("c128_decode_b2", None),                    # grid-split plan: the combine kernel
+    ("c4_prefill", list(range(0, 4096, 8)) + [1023, 1024, 4095]),
 ])
-def test_full_size_sampled(attn, name, tokens):
+def test_full_size(attn, name, tokens):
     inp = synth.make_inputs(name, device="cuda")
     run_and_compare(attn, inp, tokens=tokens)
+
+
+@pytest.mark.parametrize("splits", [4, 16])
+def test_c128_long_slices(attn, splits):
+    # one token at 1M context: 8192 compressed rows + the window, cut into
+    # slices of about 2080 keys (44 tiles) or 520 keys over 2 cluster groups
+    inp = small("c128", 128, (1048576,), seed=61)
+    run_and_compare(attn, inp, num_splits=splits)
+
+
+def test_more_tokens_than_a_grid_row(attn):
+    # one call with 70000 query tokens (two extend chunks of 35000): tokens
+    # beyond 65535 are addressed like the others
+    work = synth.Workload("t_many", batch=2, heads=8, ratio=0, seq_lens=(40000, 38000), qlen=35000,
+                          swa_resident="all", seed=62)
+    inp = synth.make_inputs(work, device="cuda")
+    assert inp.T == 70000
+    run_and_compare(attn, inp, tokens=[0, 34999, 35000, 65534, 65535, 65536, 69999])
 
 
 # ---------------------------------------------------------------- packed FP8 KV
@@ -190,9 +209,12 @@ def test_fp8_h128(attn):
     run_and_compare(attn, small("c128", 128, (700, 3000), kv_format="fp8", seed=81))
 
 
-def test_full_size_c4_verify_fp8_sampled(attn):
+def test_full_size_c4_verify_fp8(attn):
     inp = synth.make_inputs("c4_verify_fp8", device="cuda")
-    run_and_compare(attn, inp, tokens=[0, 3, 130, 255])
+    # every request's first and last query token, and all four of every 8th request
+    toks = sorted(set([4 * b for b in range(64)] + [4 * b + 3 for b in range(64)] +
+                      [4 * b + i for b in range(0, 64, 8) for i in range(4)]))
+    run_and_compare(attn, inp, tokens=toks)
 
 
 def test_back_to_back_calls_read_inputs_after_the_previous_kernel(attn):
