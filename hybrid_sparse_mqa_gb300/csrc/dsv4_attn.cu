@@ -57,18 +57,24 @@ constexpr int kRing = 2 * kRingHalf;
 constexpr int kSoftmaxWarps = 4;
 constexpr int kLoadWarps = 8;
 constexpr int kLoadThreads = kLoadWarps * 32;
-constexpr int kQkWarp = kSoftmaxWarps + kLoadWarps;   // S = Q K^T over dims 0..255 (owns the TMEM allocation);
-                                                      // warp kQkWarp + 1 takes dims 256..511
-constexpr int kPvWarp = kQkWarp + 2;                  // issues O^T += V^T P^T
-constexpr int kEpiWarp = kPvWarp + 1;                 // second PV issuer (value tiles 2, 3)
-constexpr int kWarps = kEpiWarp + 1;
+constexpr int kMmaWarp0 = kSoftmaxWarps + kLoadWarps; // four MMA issuer warps: warp kMmaWarp0 + q issues
+                                                      // S over dims 128 q .. 128 q + 127 and O^T for
+                                                      // value dims 128 q .. (warp kMmaWarp0 owns TMEM)
+constexpr int kMmaWarps = 4;
+constexpr int kQkWarp = kMmaWarp0;                    // the TMEM owner / dealloc warp
+constexpr int kWarps = kMmaWarp0 + kMmaWarps;
+// registers per thread: the launch budget, and the packed-FP8 key loop's split
+constexpr uint32_t kRegsPerThread = 128;
+constexpr uint32_t kFp8SoftmaxRegs = 112, kFp8LoadRegs = 152, kFp8IssueRegs = 96;
+static_assert(4 * kFp8SoftmaxRegs + 8 * kFp8LoadRegs + 4 * kFp8IssueRegs <= 16 * kRegsPerThread,
+              "the FP8 register split fits in the launch's registers");
 constexpr int kThreads = kWarps * 32;
 static_assert(kWarps == 16, "one O^T read-out job (TMEM quadrant, value tile) per warp");
 constexpr int kMaxCluster = 8;
 constexpr float kRescaleLog2 = 8.0f; // lazy rescale threshold (factor 256)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;       // score halves: buffer b, dim half d at column 96 b + 48 d
+constexpr uint32_t kTmemS = 0;       // scores, one partial sum per dim quarter q at column 48 q
 constexpr uint32_t kTmemO = 256;     // O^T: 4 x 64 columns, value dim 128*m + lane
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -97,8 +103,8 @@ enum Bar {
     B_KV_EMPTY = B_KV_FULL + kStages,
     B_MASK_FULL = B_KV_EMPTY + kStages,
     B_S_FULL = B_MASK_FULL + kStages,
-    B_S_FREE = B_S_FULL + 2,
-    B_P_FULL = B_S_FREE + 2,
+    B_S_FREE = B_S_FULL + 1,
+    B_P_FULL = B_S_FREE + 1,
     B_P_FREE = B_P_FULL + 2,
     B_O_FINAL = B_P_FREE + 2,
     B_MERGE,                                   // peers' partials staged by bulk copy
@@ -192,7 +198,7 @@ struct TokenInfo {
     int trow, pos, n_swa, n_c, n_extra, e0, ne, w0, nw, ntiles;
 };
 
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int* abort_flag) {
+__device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, int* abort_flag) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try(bar, parity)) return true;
@@ -206,12 +212,20 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int* abort
         }
     }
 }
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int* abort_flag) {
+    return wait_spin(bar, parity, abort_flag);
+}
 // Bounded wait on an mbarrier phase.  On time-out it records the error, marks
 // the CTA aborted and returns; callers carry on (and keep arriving on the
 // barriers others wait for), so every role reaches the end of the kernel.
+// The spin is one shared out-of-line function (less code to fetch) unless the
+// caller runs at a register count changed by setmaxnreg: a called function
+// has a single register count, so there it is inlined.
+template <bool kOutOfLine>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int* abort_flag) {
     if (mbar_try(bar, parity)) return true;
-    return wait_slow(bar, parity, abort_flag);
+    if constexpr (kOutOfLine) return wait_slow(bar, parity, abort_flag);
+    else return wait_spin(bar, parity, abort_flag);
 }
 
 // Query token t -> request row, position and the slots of slice `split`.
@@ -327,6 +341,7 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
 
 template <int KV_FORMAT>
 __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_constant__ Params p) {
+    constexpr bool kOutOfLineWait = KV_FORMAT == DSV4_KV_BF16;   // FP8 changes register counts
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
     uint8_t* smem = smem_raw;
@@ -368,20 +383,20 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     // read of an input waits for its completion.  The barriers are set up by
     // the PV issuer warp, idle until the first probabilities, so that the
     // threads whose loads start the gather are not delayed by it.
-    if (tid == kPvWarp * 32) {
+    if (tid == (kMmaWarp0 + 2) * 32) {
         mbar_init(bar(B_Q_FULL), kSoftmaxWarps * 32);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(B_KV_FULL + s), kLoadThreads);
-            mbar_init(bar(B_KV_EMPTY + s), 2);             // both PV issuers
+            mbar_init(bar(B_KV_EMPTY + s), kMmaWarps);     // every value tile's PV
             mbar_init(bar(B_MASK_FULL + s), 1);
         }
+        mbar_init(bar(B_S_FULL), kMmaWarps);                // every dim quarter of S
+        mbar_init(bar(B_S_FREE), kSoftmaxWarps * 32);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(B_S_FULL + s), 2);
-            mbar_init(bar(B_S_FREE + s), kSoftmaxWarps * 32);
             mbar_init(bar(B_P_FULL + s), kSoftmaxWarps * 32);
-            mbar_init(bar(B_P_FREE + s), 2);
+            mbar_init(bar(B_P_FREE + s), kMmaWarps);
         }
-        mbar_init(bar(B_O_FINAL), 2);
+        mbar_init(bar(B_O_FINAL), kMmaWarps);
         mbar_init(bar(B_MERGE), 1);
         fence_mbar_init_cluster();
         *abort_flag = 0;
@@ -440,9 +455,16 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     const uint32_t tmem = *tmem_slot;
     const int ntiles = ti.ntiles;
     if (tid == 0) DSV4_TR(1);
+    // Packed FP8: the loader warpgroups hold two tiles' raw rows, so during
+    // the key loop they take registers from the MMA issuer warpgroup (which
+    // needs few): 4 x 128 (softmax) + 8 x 176 (loaders) + 4 x 32 (issuers)
+    // warps' worth <= the 16 x 128 the CTA is launched with.
+    // Each role changes its budget inside its own branch and restores it
+    // before the branches join, so every instruction has one register count.
 
     if (is_loader) {
         // ============================================================ loader
+        if constexpr (KV_FORMAT != DSV4_KV_BF16) setmaxnreg_inc<kFp8LoadRegs>();
         const int lw = lt >> 5;
         if (p.debug_rows != nullptr && grp == 0) {
             // this slice's key slots (slice 0 also marks the unused tail)
@@ -497,12 +519,11 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             if (lt == 0) DSV4_TR(3);
         }
         constexpr int kR = kTileN / kLoadWarps;          // rows per loader warp
-        for (int i = 0; i < ntiles; ++i) {
-            const int stage = i % kStages, use = i / kStages;
-            const int c = i >> 2;
-            if ((i & 3) == 0 && i > 0) named_barrier_sync(1, kLoadThreads);   // chunk c resolved
+        // before tile i's ring entries are read: chunk c's barrier, and chunk
+        // 0's deferred window rows
+        auto ring_ready = [&](int i) {
+            if ((i & 3) == 0 && i > 0) named_barrier_sync(1, kLoadThreads);   // chunk i / 4 resolved
             if (i == win_tile) {
-                // chunk 0's window slots
                 const int v = lt - shift;
                 if (lt < kRingHalf && v >= ti.ne && v < nv) {
                     int row = -1;
@@ -512,12 +533,46 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 }
                 named_barrier_sync(1, kLoadThreads);
             }
-            const int v0 = i * kTileN - shift;                                // virtual slot of row 0 (may be padding)
-            const int* rg = ring + (c & 1) * kRingHalf + (i & 3) * kTileN;   // this tile's rows
-            const uint32_t dst_stage = sKV + stage * kStageBytes;
-            if constexpr (KV_FORMAT == DSV4_KV_BF16) {
+        };
+        auto tile_rows = [&](int i) { return ring + ((i >> 2) & 1) * kRingHalf + (i & 3) * kTileN; };
+        // validity of tile i's key slots as a 64-bit mask (warp 0's lanes:
+        // lane l checks rows l and 32 + l); read from the ring together with
+        // the tile's rows
+        auto tile_mask = [&](int i) -> uint64_t {
+            const int v0 = i * kTileN - shift;
+            const int* rg = tile_rows(i);
+            const bool ok0 = v0 + lane >= 0 && v0 + lane < nv && rg[lane] >= 0;
+            const bool ok1 = lane + 32 < kTileN && v0 + lane + 32 >= 0 && v0 + lane + 32 < nv && rg[lane + 32] >= 0;
+            const unsigned b0 = __ballot_sync(0xffffffffu, ok0);
+            const unsigned b1 = __ballot_sync(0xffffffffu, ok1);
+            return static_cast<uint64_t>(b0) | (static_cast<uint64_t>(b1) << 32);
+        };
+        // warp 0 publishes tile i's mask once the tile is on its way; then
+        // the next chunk's rows are resolved once this chunk's first two
+        // tiles are issued (ring half (c + 1) & 1 was last read by chunk
+        // c - 1, whose rows and masks every loader has read before the
+        // barrier that opens chunk c)
+        auto publish_mask = [&](int i, uint64_t mask) {
+            if (lane == 0) {
+                const int stage = i % kStages;
+                *reinterpret_cast<volatile uint64_t*>(smem + OFF_MASK + stage * 8) = mask;
+                mbar_arrive(bar(B_MASK_FULL + stage));
+            }
+        };
+        auto tile_tail = [&](int i) {
+            if (lt == 0 && i < 8) DSV4_TR(4 + i);
+            const int c = i >> 2;
+            if ((i & 3) == 1 && (c + 1) * kRingHalf < nv + shift) resolve_chunk(c + 1);
+        };
+        if constexpr (KV_FORMAT == DSV4_KV_BF16) {
+            for (int i = 0; i < ntiles; ++i) {
+                const int stage = i % kStages, use = i / kStages;
+                ring_ready(i);
+                const int v0 = i * kTileN - shift;                                // virtual slot of row 0 (may be padding)
+                const int* rg = tile_rows(i);
+                const uint32_t dst_stage = sKV + stage * kStageBytes;
                 if (i >= kStages) {
-                    wait_bar(bar(B_KV_EMPTY + stage), (use - 1) & 1, abort_flag);
+                    wait_bar<kOutOfLineWait>(bar(B_KV_EMPTY + stage), (use - 1) & 1, abort_flag);
                     fence_proxy_async();
                 }
 #pragma unroll
@@ -534,48 +589,59 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                     }
                 }
                 cp_async_arrive_noinc(bar(B_KV_FULL + stage));
-            } else {
-                // packed FP8 rows: lane l < 28 dequantises nope dims 16l..16l+15
-                // (e4m3 x the fp32 scale of their 64-dim block, rounded to bf16);
-                // lanes 28..31 copy 16 dims of the bf16 rope each.  The raw
-                // bytes are loaded before the stage is free.
-                uint4 raw[kR], raw2[kR];
-                float scl[kR];
+                if (lw == 0) publish_mask(i, tile_mask(i));
+                tile_tail(i);
+            }
+        } else {
+            // Packed FP8 rows: lane l < 28 dequantises nope dims 16l..16l+15
+            // (e4m3 x the fp32 scale of their 64-dim block, rounded to bf16);
+            // lanes 28..31 copy 16 dims of the bf16 rope each.  Two register
+            // sets: the raw bytes of tile i + 1 are loaded before tile i is
+            // dequantised (this warpgroup runs with a raised register budget).
+            struct Raw { uint4 a[kR], b[kR]; float scl[kR]; uint64_t mask; };
+            auto fp8_load = [&](Raw& x, int i) {
+                const int v0 = i * kTileN - shift;
+                const int* rg = tile_rows(i);
+                x.mask = lw == 0 ? tile_mask(i) : 0;
 #pragma unroll
                 for (int k = 0; k < kR; ++k) {
                     const int r = lw * kR + k;
                     const int v = v0 + r;
                     const int row = (v >= 0 && v < nv) ? rg[r] : -1;
-                    raw[k] = raw2[k] = make_uint4(0, 0, 0, 0);
-                    scl[k] = 0.f;
+                    x.a[k] = x.b[k] = make_uint4(0, 0, 0, 0);
+                    x.scl[k] = 0.f;
                     if (row >= 0) {
                         const uint8_t* src = slot_row_ptr(p, ti, v, row);
                         if (lane < 28) {
-                            raw[k] = __ldg(reinterpret_cast<const uint4*>(src + lane * 16));
-                            scl[k] = __ldg(reinterpret_cast<const float*>(src + kFp8ScaleOff) + (lane >> 2));
+                            x.a[k] = __ldg(reinterpret_cast<const uint4*>(src + lane * 16));
+                            x.scl[k] = __ldg(reinterpret_cast<const float*>(src + kFp8ScaleOff) + (lane >> 2));
                         } else {
                             const uint4* rp = reinterpret_cast<const uint4*>(src + kFp8NopeBytes + (lane - 28) * 32);
-                            raw[k] = __ldg(rp);
-                            raw2[k] = __ldg(rp + 1);
+                            x.a[k] = __ldg(rp);
+                            x.b[k] = __ldg(rp + 1);
                         }
                     }
                 }
+            };
+            auto fp8_store = [&](const Raw& x, int i) {
+                const int stage = i % kStages, use = i / kStages;
+                const uint32_t dst_stage = sKV + stage * kStageBytes;
                 if (i >= kStages) {
-                    wait_bar(bar(B_KV_EMPTY + stage), (use - 1) & 1, abort_flag);
+                    wait_bar<kOutOfLineWait>(bar(B_KV_EMPTY + stage), (use - 1) & 1, abort_flag);
                     fence_proxy_async();
                 }
 #pragma unroll
                 for (int k = 0; k < kR; ++k) {
                     const int r = lw * kR + k;
                     if (lane < 28) {
-                        const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+                        const uint32_t w[4] = {x.a[k].x, x.a[k].y, x.a[k].z, x.a[k].w};
                         uint32_t o[8];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             float f[4];
                             e4m3x4_to_f32(w[e], f);
-                            o[2 * e] = pack_bf16x2(f[0] * scl[k], f[1] * scl[k]);
-                            o[2 * e + 1] = pack_bf16x2(f[2] * scl[k], f[3] * scl[k]);
+                            o[2 * e] = pack_bf16x2(f[0] * x.scl[k], f[1] * x.scl[k]);
+                            o[2 * e + 1] = pack_bf16x2(f[2] * x.scl[k], f[3] * x.scl[k]);
                         }
                         const uint32_t cbase = dst_stage + (lane >> 2) * kChunkKV;
                         st_shared_v4(cbase + sw128(r, 2 * (lane & 3)), o[0], o[1], o[2], o[3]);
@@ -583,95 +649,119 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                     } else {
                         const uint32_t cbase = dst_stage + 7 * kChunkKV;
                         const int j = 2 * (lane - 28);
-                        st_shared_v4(cbase + sw128(r, j), raw[k].x, raw[k].y, raw[k].z, raw[k].w);
-                        st_shared_v4(cbase + sw128(r, j + 1), raw2[k].x, raw2[k].y, raw2[k].z, raw2[k].w);
+                        st_shared_v4(cbase + sw128(r, j), x.a[k].x, x.a[k].y, x.a[k].z, x.a[k].w);
+                        st_shared_v4(cbase + sw128(r, j + 1), x.b[k].x, x.b[k].y, x.b[k].z, x.b[k].w);
                     }
                 }
                 fence_proxy_async();
                 mbar_arrive(bar(B_KV_FULL + stage));
+                if (lw == 0) publish_mask(i, x.mask);
+                tile_tail(i);
+            };
+            Raw ra, rb;
+            if (ntiles > 0) {
+                ring_ready(0);
+                fp8_load(ra, 0);
             }
-            if (lw == 0) {
-                // validity of the tile's key slots (lane l: rows l and 32 + l)
-                const bool ok0 = v0 + lane >= 0 && v0 + lane < nv && rg[lane] >= 0;
-                const bool ok1 = lane + 32 < kTileN && v0 + lane + 32 >= 0 && v0 + lane + 32 < nv && rg[lane + 32] >= 0;
-                const unsigned b0 = __ballot_sync(0xffffffffu, ok0);
-                const unsigned b1 = __ballot_sync(0xffffffffu, ok1);
-                if (lane == 0) {
-                    *reinterpret_cast<volatile uint64_t*>(smem + OFF_MASK + stage * 8) =
-                        static_cast<uint64_t>(b0) | (static_cast<uint64_t>(b1) << 32);
-                    mbar_arrive(bar(B_MASK_FULL + stage));
+            for (int i = 0; i < ntiles; i += 2) {
+                if (i + 1 < ntiles) {
+                    ring_ready(i + 1);
+                    fp8_load(rb, i + 1);
+                }
+                fp8_store(ra, i);
+                if (i + 1 < ntiles) {
+                    if (i + 2 < ntiles) {
+                        ring_ready(i + 2);
+                        fp8_load(ra, i + 2);
+                    }
+                    fp8_store(rb, i + 1);
                 }
             }
-            if (lt == 0 && i < 8) DSV4_TR(4 + i);
-            // resolve the next chunk once this one's first two tiles are on their way
-            // (ring half (c + 1) & 1 was last read by chunk c - 1, finished by all)
-            if ((i & 3) == 1 && (c + 1) * kRingHalf < nv + shift) resolve_chunk(c + 1);
         }
         cp_async_wait_all();
-    } else if (warp == kQkWarp || warp == kQkWarp + 1) {
-        // ============================================================ S = Q K^T issuers
-        // warp kQkWarp + d accumulates dims 256 d .. 256 d + 255 into its own
-        // score half; softmax adds the halves
-        const int dh = warp - kQkWarp;
+        if constexpr (KV_FORMAT != DSV4_KV_BF16) setmaxnreg_dec<kRegsPerThread>();
+    } else if (warp >= kMmaWarp0) {
+        // ============================================================ MMA issuers
+        if constexpr (KV_FORMAT != DSV4_KV_BF16) setmaxnreg_dec<kFp8IssueRegs>();
+        // Warp kMmaWarp0 + q issues, for every tile, S = Q K^T over dims
+        // 128 q .. 128 q + 127 into its own partial score sum (the softmax adds
+        // the four), and O^T += V^T P^T for value dims 128 q .. 128 q + 127
+        // (M = 128 value dims, N = 64 heads, K = 48 keys; A = the same KV
+        // stage read MN-major).  A tcgen05.mma costs its issuing thread about
+        // as long as a small MMA runs, so four issuers keep the tensor pipe fed.
+        // S of tile i needs the tile's rows and the softmax to have read S of
+        // tile i - 1 (one score buffer); PV of tile j needs its probabilities.
+        const int mq = warp - kMmaWarp0;
         if (lane == 0 && ntiles > 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kHG, kTileN, false, false);
-            wait_bar(bar(B_Q_FULL), 0, abort_flag);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kHG, true, false);
+            wait_bar<kOutOfLineWait>(bar(B_Q_FULL), 0, abort_flag);
             fence_proxy_async();
             tc_fence_after();
-            for (int i = 0; i < ntiles; ++i) {
-                const int stage = i % kStages, use = i / kStages;
-                wait_bar(bar(B_KV_FULL + stage), use & 1, abort_flag);
-                if (i >= 2) wait_bar(bar(B_S_FREE + (i & 1)), ((i - 2) >> 1) & 1, abort_flag);
-                if (dh == 0 && i < 8) DSV4_TR(12 + i);
+            // S of tile i and PV of tile i - 1 are issued in whichever order
+            // their inputs are ready (PV must not wait for the next tile's rows)
+            auto issue_s = [&](int i) {
+                const int stage = i % kStages;
+                if (mq == 0 && i < 8) DSV4_TR(12 + i);
                 fence_proxy_async();
                 tc_fence_after();
                 const uint32_t stg = sKV + stage * kStageBytes;
-                const uint32_t dcol = tmem + kTmemS + (i & 1) * (2 * kTileN) + dh * kTileN;
+                const uint32_t dcol = tmem + kTmemS + mq * kTileN;
 #pragma unroll
-                for (int kq = 0; kq < 16; ++kq) {
-                    const int k = 16 * dh + kq;
+                for (int kq = 0; kq < 8; ++kq) {
+                    const int k = 8 * mq + kq;
                     const uint64_t a = smem_desc_sw128(sQ + (k >> 2) * kChunkQ + (k & 3) * 32, 16, 1024);
                     const uint64_t b = smem_desc_sw128(stg + (k >> 2) * kChunkKV + (k & 3) * 32, 16, 1024);
                     mma_bf16_ss(dcol, a, b, idesc_qk, kq > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(B_S_FULL + (i & 1)));
-            }
-        }
-        __syncwarp();
-    } else if (warp == kPvWarp || warp == kEpiWarp) {
-        // ============================================================ O^T += V^T P^T issuers
-        // two warps, each over two of the four 128-dim value tiles: a
-        // tcgen05.mma costs its issuing thread about as long as it runs
-        if (lane == 0 && ntiles > 0) {
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kHG, true, false);
-            const int mt0 = warp == kPvWarp ? 0 : 2;
-            for (int i = 0; i < ntiles; ++i) {
-                const int stage = i % kStages;
-                wait_bar(bar(B_P_FULL + (i & 1)), (i >> 1) & 1, abort_flag);
-                if (i < 8 && mt0 == 0) DSV4_TR(20 + i);
+                mma_commit(bar(B_S_FULL));
+            };
+            auto issue_pv = [&](int j) {
+                const int stage = j % kStages;
+                if (j < 8 && mq == 0) DSV4_TR(20 + j);
                 tc_fence_after();
                 const uint32_t stg = sKV + stage * kStageBytes;
-                const uint32_t pbuf = sP + (i & 1) * kPBytes;
+                const uint32_t pbuf = sP + (j & 1) * kPBytes;
 #pragma unroll
-                for (int m2 = 0; m2 < 2; ++m2) {
-                    const int mt = mt0 + m2;
-#pragma unroll
-                    for (int kk = 0; kk < kTileN / 16; ++kk) {
-                        // A = V^T (dims 128*mt.., keys 16*kk..): MN-major, 64-dim atoms one chunk apart
-                        const uint64_t a = smem_desc_sw128(stg + 2 * mt * kChunkKV + kk * 2048, kChunkKV, 1024);
-                        // B = P (heads x keys), K-major
-                        const uint64_t b = smem_desc_sw128(pbuf + kk * 32, 16, 1024);
-                        mma_bf16_ss(tmem + kTmemO + mt * kHG, a, b, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kTileN / 16; ++kk) {
+                    // A = V^T (dims 128*mq.., keys 16*kk..): MN-major, 64-dim atoms one chunk apart
+                    const uint64_t a = smem_desc_sw128(stg + 2 * mq * kChunkKV + kk * 2048, kChunkKV, 1024);
+                    // B = P (heads x keys), K-major
+                    const uint64_t b = smem_desc_sw128(pbuf + kk * 32, 16, 1024);
+                    mma_bf16_ss(tmem + kTmemO + mq * kHG, a, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(bar(B_P_FREE + (j & 1)));
+                mma_commit(bar(B_KV_EMPTY + stage));
+            };
+            int ns = 0, np = 0;                    // S issued for tiles < ns, PV for tiles < np
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t it = 1; np < ntiles; ++it) {
+                bool progress = false;
+                if (ns < ntiles && mbar_test(bar(B_KV_FULL + ns % kStages), (ns / kStages) & 1) &&
+                    (ns == 0 || mbar_test(bar(B_S_FREE), (ns - 1) & 1))) {
+                    issue_s(ns++);
+                    progress = true;
+                }
+                if (np < ns && mbar_test(bar(B_P_FULL + (np & 1)), (np >> 1) & 1)) {
+                    issue_pv(np++);
+                    progress = true;
+                }
+                if (!progress && (it & 63u) == 0) {
+                    if (*reinterpret_cast<volatile int*>(abort_flag)) break;
+                    if (globaltimer_ns() - t0 > kTimeoutNs) {
+                        atomicOr(&g_dev_error, DSV4_DEV_ERR_TIMEOUT);
+                        *reinterpret_cast<volatile int*>(abort_flag) = 1;
+                        break;
                     }
                 }
-                mma_commit(bar(B_P_FREE + (i & 1)));
-                mma_commit(bar(B_KV_EMPTY + stage));
             }
             mma_commit(bar(B_O_FINAL));
         }
         __syncwarp();
+        if constexpr (KV_FORMAT != DSV4_KV_BF16) setmaxnreg_inc<kRegsPerThread>();
     } else if (warp < kSoftmaxWarps) {
         // ============================================================ softmax
+        if constexpr (KV_FORMAT != DSV4_KV_BF16) setmaxnreg_dec<kFp8SoftmaxRegs>();
         // Q rows of this head group (1 KB each), zero past the last head
         {
             const uint8_t* qb = reinterpret_cast<const uint8_t*>(p.q) + ((size_t)t * p.H + head0) * 1024;
@@ -700,14 +790,14 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             const int sb = i & 1;
             const int stage = i % kStages, use = i / kStages;
             float s[kJ];
-            wait_bar(bar(B_S_FULL + sb), (i >> 1) & 1, abort_flag);
+            wait_bar<kOutOfLineWait>(bar(B_S_FULL), i & 1, abort_flag);
             if (tid == 0 && i < 8) DSV4_TR(28 + i);
             __syncwarp();
             tc_fence_after();
-            tmem_ld16x64b_48_sum2(lane_addr + kTmemS + sb * (2 * kTileN), lane_addr + kTmemS + sb * (2 * kTileN) + kTileN, s);
+            tmem_ld16x64b_48_sum4(lane_addr + kTmemS, s);
             tc_fence_before();
-            mbar_arrive(bar(B_S_FREE + sb));
-            wait_bar(bar(B_MASK_FULL + stage), use & 1, abort_flag);
+            mbar_arrive(bar(B_S_FREE));
+            wait_bar<kOutOfLineWait>(bar(B_MASK_FULL + stage), use & 1, abort_flag);
             const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + OFF_MASK + stage * 8) >> par;
             float tmax = -INFINITY;
 #pragma unroll
@@ -754,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 if (bar_red_or(2, kSoftmaxWarps * 32, need)) {
                     if (owner) wsm[h] = alpha;
                     named_barrier_sync(2, kSoftmaxWarps * 32);
-                    wait_bar(bar(B_P_FREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag);
+                    wait_bar<kOutOfLineWait>(bar(B_P_FREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag);
                     __syncwarp();
                     tc_fence_after();
 #pragma unroll 1
@@ -767,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                     }
                 }
             }
-            if (i >= 2) wait_bar(bar(B_P_FREE + sb), ((i - 2) >> 1) & 1, abort_flag);
+            if (i >= 2) wait_bar<kOutOfLineWait>(bar(B_P_FREE + sb), ((i - 2) >> 1) & 1, abort_flag);
             {
                 const uint32_t prow = sP + sb * kPBytes;
 #pragma unroll
@@ -784,6 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         const float l_all = l_run + __shfl_xor_sync(0xffffffffu, l_run, 2);
         if (owner) ml[h] = make_float2(live && ntiles > 0 ? m_run : -INFINITY, live && ntiles > 0 ? l_all : 0.f);
         fence_proxy_async();
+        if constexpr (KV_FORMAT != DSV4_KV_BF16) setmaxnreg_inc<kRegsPerThread>();
     }
 
     // ------------------------------------------------------------ epilogue
@@ -877,7 +968,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     const bool owned = d >= dbase && d < dbase + nd;
     float o[kHG];
     if (ntiles > 0) {
-        wait_bar(bar(B_O_FINAL), 0, abort_flag);
+        wait_bar<kOutOfLineWait>(bar(B_O_FINAL), 0, abort_flag);
         if (tid == 0) DSV4_TR(52);
         tc_fence_after();
         fence_proxy_async();
@@ -960,7 +1051,7 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 "l"(mrg_ml), "r"(static_cast<uint32_t>(Sc * kHG * 8)), "r"(mb)
                 : "memory");
         }
-        wait_bar(bar(B_MERGE), 0, abort_flag);
+        wait_bar<kOutOfLineWait>(bar(B_MERGE), 0, abort_flag);
         if (tid == 0) DSV4_TR(59);
         if (warp < 4 && lane < 16) merge_weights();
         __syncthreads();

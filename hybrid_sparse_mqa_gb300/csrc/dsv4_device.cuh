@@ -177,6 +177,17 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) 
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Per-warpgroup register budget (every warp of the warpgroup executes it):
+// dec releases registers to the CTA's pool, inc waits for and takes them.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -322,6 +333,15 @@ __device__ __forceinline__ void tmem_ld16x64b_48_sum2(uint32_t a0, uint32_t a1, 
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) + __uint_as_float(r[16 + i]);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[16 + i] = __uint_as_float(q[i]) + __uint_as_float(q[8 + i]);
+}
+// The same over four accumulators at a, a + 48, a + 96, a + 144 (the four
+// dim quarters of a split product), added.
+__device__ __forceinline__ void tmem_ld16x64b_48_sum4(uint32_t a, float (&v)[24]) {
+    float u[24];
+    tmem_ld16x64b_48_sum2(a, a + 48u, v);
+    tmem_ld16x64b_48_sum2(a + 96u, a + 144u, u);
+#pragma unroll
+    for (int i = 0; i < 24; ++i) v[i] += u[i];
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
     asm volatile(
