@@ -63,12 +63,10 @@ constexpr int kMmaWarp0 = kSoftmaxWarps + kLoadWarps; // four MMA issuer warps: 
 constexpr int kMmaWarps = 4;
 constexpr int kQkWarp = kMmaWarp0;                    // the TMEM owner / dealloc warp
 constexpr int kWarps = kMmaWarp0 + kMmaWarps;
-// registers per thread: the launch budget, and the packed-FP8 key loop's split
-constexpr uint32_t kRegsPerThread = 128;
-constexpr uint32_t kFp8SoftmaxRegs = 112, kFp8LoadRegs = 152, kFp8IssueRegs = 96;
-static_assert(4 * kFp8SoftmaxRegs + 8 * kFp8LoadRegs + 4 * kFp8IssueRegs <= 16 * kRegsPerThread,
-              "the FP8 register split fits in the launch's registers");
 constexpr int kThreads = kWarps * 32;
+// packed FP8: loader warps 0..5 dequantise (8 key rows each), 6 and 7 issue the row copies
+constexpr int kFp8DqWarps = 6;
+constexpr int kFp8DqThreads = kFp8DqWarps * 32;
 static_assert(kWarps == 16, "one O^T read-out job (TMEM quadrant, value tile) per warp");
 constexpr int kMaxCluster = 8;
 constexpr float kRescaleLog2 = 8.0f; // lazy rescale threshold (factor 256)
@@ -102,7 +100,8 @@ enum Bar {
     B_KV_FULL = 1,
     B_KV_EMPTY = B_KV_FULL + kStages,
     B_MASK_FULL = B_KV_EMPTY + kStages,
-    B_S_FULL = B_MASK_FULL + kStages,
+    B_RAW_FULL = B_MASK_FULL + kStages,        // packed FP8: a tile's raw rows landed
+    B_S_FULL = B_RAW_FULL + kStages,
     B_S_FREE = B_S_FULL + 1,
     B_P_FULL = B_S_FREE + 1,
     B_P_FREE = B_P_FULL + 2,
@@ -218,9 +217,9 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int* abort
 // Bounded wait on an mbarrier phase.  On time-out it records the error, marks
 // the CTA aborted and returns; callers carry on (and keep arriving on the
 // barriers others wait for), so every role reaches the end of the kernel.
-// The spin is one shared out-of-line function (less code to fetch) unless the
-// caller runs at a register count changed by setmaxnreg: a called function
-// has a single register count, so there it is inlined.
+// The spin is one shared out-of-line function (less code to fetch) or, where
+// the caller keeps many values live across the wait and a call would make it
+// save them, inlined.
 template <bool kOutOfLine>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int* abort_flag) {
     if (mbar_try(bar, parity)) return true;
@@ -341,7 +340,7 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
 
 template <int KV_FORMAT>
 __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_constant__ Params p) {
-    constexpr bool kOutOfLineWait = KV_FORMAT == DSV4_KV_BF16;   // FP8 changes register counts
+    constexpr bool kOutOfLineWait = KV_FORMAT == DSV4_KV_BF16;   // the FP8 loader inlines its waits
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
     uint8_t* smem = smem_raw;
@@ -386,9 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     if (tid == (kMmaWarp0 + 2) * 32) {
         mbar_init(bar(B_Q_FULL), kSoftmaxWarps * 32);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(B_KV_FULL + s), kLoadThreads);
+            mbar_init(bar(B_KV_FULL + s), KV_FORMAT == DSV4_KV_BF16 ? kLoadThreads : kFp8DqThreads);
             mbar_init(bar(B_KV_EMPTY + s), kMmaWarps);     // every value tile's PV
-            mbar_init(bar(B_MASK_FULL + s), 1);
+            mbar_init(bar(B_MASK_FULL + s), KV_FORMAT == DSV4_KV_BF16 ? 1 : 2);   // FP8: one per issuer warp
+            mbar_init(bar(B_RAW_FULL + s), 2);
         }
         mbar_init(bar(B_S_FULL), kMmaWarps);                // every dim quarter of S
         mbar_init(bar(B_S_FREE), kSoftmaxWarps * 32);
@@ -459,12 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     // the key loop they take registers from the MMA issuer warpgroup (which
     // needs few): 4 x 128 (softmax) + 8 x 176 (loaders) + 4 x 32 (issuers)
     // warps' worth <= the 16 x 128 the CTA is launched with.
-    // Each role changes its budget inside its own branch and restores it
-    // before the branches join, so every instruction has one register count.
-
     if (is_loader) {
         // ============================================================ loader
-        if constexpr (KV_FORMAT != DSV4_KV_BF16) setmaxnreg_inc<kFp8LoadRegs>();
         const int lw = lt >> 5;
         if (p.debug_rows != nullptr && grp == 0) {
             // this slice's key slots (slice 0 also marks the unused tail)
@@ -593,96 +589,120 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 tile_tail(i);
             }
         } else {
-            // Packed FP8 rows: lane l < 28 dequantises nope dims 16l..16l+15
-            // (e4m3 x the fp32 scale of their 64-dim block, rounded to bf16);
-            // lanes 28..31 copy 16 dims of the bf16 rope each.  Two register
-            // sets: the raw bytes of tile i + 1 are loaded before tile i is
-            // dequantised (this warpgroup runs with a raised register budget).
-            struct Raw { uint4 a[kR], b[kR]; float scl[kR]; uint64_t mask; };
-            auto fp8_load = [&](Raw& x, int i) {
-                const int v0 = i * kTileN - shift;
-                const int* rg = tile_rows(i);
-                x.mask = lw == 0 ? tile_mask(i) : 0;
-#pragma unroll
-                for (int k = 0; k < kR; ++k) {
-                    const int r = lw * kR + k;
-                    const int v = v0 + r;
-                    const int row = (v >= 0 && v < nv) ? rg[r] : -1;
-                    x.a[k] = x.b[k] = make_uint4(0, 0, 0, 0);
-                    x.scl[k] = 0.f;
-                    if (row >= 0) {
-                        const uint8_t* src = slot_row_ptr(p, ti, v, row);
-                        if (lane < 28) {
-                            x.a[k] = __ldg(reinterpret_cast<const uint4*>(src + lane * 16));
-                            x.scl[k] = __ldg(reinterpret_cast<const float*>(src + kFp8ScaleOff) + (lane >> 2));
-                        } else {
-                            const uint4* rp = reinterpret_cast<const uint4*>(src + kFp8NopeBytes + (lane - 28) * 32);
-                            x.a[k] = __ldg(rp);
-                            x.b[k] = __ldg(rp + 1);
-                        }
+            // Packed FP8 rows.  Loader warps 6 and 7 copy them, two tiles
+            // ahead: each 608-byte row by one bulk copy into the top of its
+            // tile's stage (rows 0..31 by warp 6, 32..47 by warp 7, which
+            // also publish the tile's key mask, one 32-bit half each).  Warps
+            // 0..5 dequantise: lane 4 k + q of warp w holds row 8 w + k,
+            // dims 64 m + 16 q .. + 15 of every 64-dim block m (e4m3 x the
+            // block's fp32 scale, rounded to bf16) and rope dims 16 q .. + 15
+            // (already bf16).  The bf16 tile overwrites the raw rows, so the
+            // six warps read all their raw bytes, meet, then write; every
+            // shared access spreads its 16-byte pieces evenly over the banks.
+            // A padded or masked row is written as zeros.
+            static_assert(kFp8DqWarps * 8 == kTileN && kLoadWarps == kFp8DqWarps + 2, "FP8 loader roles");
+            constexpr uint32_t kRawOff = kStageBytes - kTileN * kFp8RowBytes;
+            static_assert(kRawOff % 16 == 0 && kFp8RowBytes % 16 == 0, "bulk copies move 16-byte units");
+            if (lw >= kFp8DqWarps) {
+                // ---------------------------------------------- row copies
+                const int r = (lw - kFp8DqWarps) * 32 + lane;   // this lane's row of every tile
+                for (int j = 0; j < ntiles; ++j) {
+                    const int stage = j % kStages;
+                    if ((j & 3) == 0 && j > 0) named_barrier_sync(1, kLoadThreads);   // chunk j / 4 resolved
+                    if (j == win_tile) named_barrier_sync(1, kLoadThreads);          // deferred window rows
+                    if (j >= kStages) {
+                        // stage j % 3 held tile j - 3 (and its mask) until its PV finished
+                        wait_bar<kOutOfLineWait>(bar(B_KV_EMPTY + stage), (j / kStages - 1) & 1, abort_flag);
+                        fence_proxy_async();
                     }
+                    const int v = j * kTileN - shift + r;
+                    const int row = (r < kTileN && v >= 0 && v < nv) ? tile_rows(j)[r] : -1;
+                    const unsigned valid = __ballot_sync(0xffffffffu, row >= 0);
+                    if (lane == 0) {
+                        reinterpret_cast<volatile uint32_t*>(smem + OFF_MASK + stage * 8)[lw - kFp8DqWarps] = valid;
+                        mbar_arrive(bar(B_MASK_FULL + stage));
+                        mbar_arrive_expect_tx(bar(B_RAW_FULL + stage), __popc(valid) * kFp8RowBytes);
+                    }
+                    __syncwarp();
+                    if (row >= 0)
+                        bulk_copy_g2s(sKV + stage * kStageBytes + kRawOff + r * kFp8RowBytes,
+                                      slot_row_ptr(p, ti, v, row), kFp8RowBytes, bar(B_RAW_FULL + stage));
                 }
-            };
-            auto fp8_store = [&](const Raw& x, int i) {
-                const int stage = i % kStages, use = i / kStages;
-                const uint32_t dst_stage = sKV + stage * kStageBytes;
-                if (i >= kStages) {
-                    wait_bar<kOutOfLineWait>(bar(B_KV_EMPTY + stage), (use - 1) & 1, abort_flag);
-                    fence_proxy_async();
+            } else {
+                // ---------------------------------------------- dequantisation
+                if (win_tile >= 0) {
+                    ring_ready(win_tile);           // enters the deferred window rows, then waits with the copiers
                 }
+                const int k = lane >> 2, q = lane & 3;
+                const int r = lw * 8 + k;
+                for (int i = 0; i < ntiles; ++i) {
+                    const int stage = i % kStages;
+                    const uint32_t dst_stage = sKV + stage * kStageBytes;
+                    const uint32_t src = dst_stage + kRawOff + r * kFp8RowBytes;
+                    wait_bar<kOutOfLineWait>(bar(B_RAW_FULL + stage), (i / kStages) & 1, abort_flag);
+                    const bool ok = (*reinterpret_cast<volatile uint64_t*>(smem + OFF_MASK + stage * 8) >> r) & 1ull;
+                    uint4 nope[7], rope[2];
+                    float scl[7];
+                    if (ok) {
 #pragma unroll
-                for (int k = 0; k < kR; ++k) {
-                    const int r = lw * kR + k;
-                    if (lane < 28) {
-                        const uint32_t w[4] = {x.a[k].x, x.a[k].y, x.a[k].z, x.a[k].w};
+                        for (int m = 0; m < 7; ++m) nope[m] = ld_shared_u4(src + (4 * m + q) * 16);
+                        rope[0] = ld_shared_u4(src + kFp8NopeBytes + q * 32);
+                        rope[1] = ld_shared_u4(src + kFp8NopeBytes + q * 32 + 16);
+                        const float4 s03 = ld_shared_v4(src + kFp8ScaleOff);
+                        const float4 s46 = ld_shared_v4(src + kFp8ScaleOff + 16);
+                        scl[0] = s03.x; scl[1] = s03.y; scl[2] = s03.z; scl[3] = s03.w;
+                        scl[4] = s46.x; scl[5] = s46.y; scl[6] = s46.z;
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < 7; ++m) { nope[m] = make_uint4(0, 0, 0, 0); scl[m] = 0.f; }
+                        rope[0] = rope[1] = make_uint4(0, 0, 0, 0);
+                    }
+                    named_barrier_sync(4, kFp8DqThreads);       // every raw row of the stage is read
+#pragma unroll
+                    for (int m = 0; m < 7; ++m) {
+                        const uint32_t w[4] = {nope[m].x, nope[m].y, nope[m].z, nope[m].w};
                         uint32_t o[8];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             float f[4];
                             e4m3x4_to_f32(w[e], f);
-                            o[2 * e] = pack_bf16x2(f[0] * x.scl[k], f[1] * x.scl[k]);
-                            o[2 * e + 1] = pack_bf16x2(f[2] * x.scl[k], f[3] * x.scl[k]);
+                            o[2 * e] = pack_bf16x2(f[0] * scl[m], f[1] * scl[m]);
+                            o[2 * e + 1] = pack_bf16x2(f[2] * scl[m], f[3] * scl[m]);
                         }
-                        const uint32_t cbase = dst_stage + (lane >> 2) * kChunkKV;
-                        st_shared_v4(cbase + sw128(r, 2 * (lane & 3)), o[0], o[1], o[2], o[3]);
-                        st_shared_v4(cbase + sw128(r, 2 * (lane & 3) + 1), o[4], o[5], o[6], o[7]);
-                    } else {
-                        const uint32_t cbase = dst_stage + 7 * kChunkKV;
-                        const int j = 2 * (lane - 28);
-                        st_shared_v4(cbase + sw128(r, j), x.a[k].x, x.a[k].y, x.a[k].z, x.a[k].w);
-                        st_shared_v4(cbase + sw128(r, j + 1), x.b[k].x, x.b[k].y, x.b[k].z, x.b[k].w);
+                        const uint32_t cb = dst_stage + m * kChunkKV;
+                        st_shared_v4(cb + sw128(r, 2 * q), o[0], o[1], o[2], o[3]);
+                        st_shared_v4(cb + sw128(r, 2 * q + 1), o[4], o[5], o[6], o[7]);
+                    }
+                    {
+                        const uint32_t cb = dst_stage + 7 * kChunkKV;
+                        st_shared_v4(cb + sw128(r, 2 * q), rope[0].x, rope[0].y, rope[0].z, rope[0].w);
+                        st_shared_v4(cb + sw128(r, 2 * q + 1), rope[1].x, rope[1].y, rope[1].z, rope[1].w);
+                    }
+                    fence_proxy_async();
+                    mbar_arrive(bar(B_KV_FULL + stage));
+                    if (lt == 0 && i < 8) DSV4_TR(4 + i);
+                    // the next chunk's rows once this chunk's first two tiles
+                    // are in: ring half (c + 1) & 1 last held chunk c - 1, whose
+                    // tiles were all copied before this tile's rows were
+                    const int c = i >> 2;
+                    if ((i & 3) == 1 && (c + 1) * kRingHalf < nv + shift) {
+                        resolve_chunk(c + 1);
+                        named_barrier_arrive(1, kLoadThreads);
                     }
                 }
-                fence_proxy_async();
-                mbar_arrive(bar(B_KV_FULL + stage));
-                if (lw == 0) publish_mask(i, x.mask);
-                tile_tail(i);
-            };
-            Raw ra, rb;
-            if (ntiles > 0) {
-                ring_ready(0);
-                fp8_load(ra, 0);
-            }
-            for (int i = 0; i < ntiles; i += 2) {
-                if (i + 1 < ntiles) {
-                    ring_ready(i + 1);
-                    fp8_load(rb, i + 1);
-                }
-                fp8_store(ra, i);
-                if (i + 1 < ntiles) {
-                    if (i + 2 < ntiles) {
-                        ring_ready(i + 2);
-                        fp8_load(ra, i + 2);
-                    }
-                    fp8_store(rb, i + 1);
+                // after an abort the waits above may have returned early: let
+                // the last copies land (bounded) before the stages are reused
+                // or the CTA exits
+                for (int j = ntiles - 1; j >= 0 && j >= ntiles - kStages; --j) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try(bar(B_RAW_FULL + j % kStages), (j / kStages) & 1))
+                        if (globaltimer_ns() - t0 > kTimeoutNs) break;
                 }
             }
         }
         cp_async_wait_all();
-        if constexpr (KV_FORMAT != DSV4_KV_BF16) setmaxnreg_dec<kRegsPerThread>();
     } else if (warp >= kMmaWarp0) {
         // ============================================================ MMA issuers
-        if constexpr (KV_FORMAT != DSV4_KV_BF16) setmaxnreg_dec<kFp8IssueRegs>();
         // Warp kMmaWarp0 + q issues, for every tile, S = Q K^T over dims
         // 128 q .. 128 q + 127 into its own partial score sum (the softmax adds
         // the four), and O^T += V^T P^T for value dims 128 q .. 128 q + 127
@@ -758,10 +778,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             mma_commit(bar(B_O_FINAL));
         }
         __syncwarp();
-        if constexpr (KV_FORMAT != DSV4_KV_BF16) setmaxnreg_inc<kRegsPerThread>();
     } else if (warp < kSoftmaxWarps) {
         // ============================================================ softmax
-        if constexpr (KV_FORMAT != DSV4_KV_BF16) setmaxnreg_dec<kFp8SoftmaxRegs>();
         // Q rows of this head group (1 KB each), zero past the last head
         {
             const uint8_t* qb = reinterpret_cast<const uint8_t*>(p.q) + ((size_t)t * p.H + head0) * 1024;
@@ -874,7 +892,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         const float l_all = l_run + __shfl_xor_sync(0xffffffffu, l_run, 2);
         if (owner) ml[h] = make_float2(live && ntiles > 0 ? m_run : -INFINITY, live && ntiles > 0 ? l_all : 0.f);
         fence_proxy_async();
-        if constexpr (KV_FORMAT != DSV4_KV_BF16) setmaxnreg_inc<kRegsPerThread>();
     }
 
     // ------------------------------------------------------------ epilogue
