@@ -1130,61 +1130,70 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
 // Merges Sg cluster results of each (token, head): the weights are
 // L_g * exp(M_g - M) with M the largest of the M_g and the sink; the sink
 // adds exp(sink - M) to the denominator and nothing to the numerator.  One
-// thread per (token, head, 8 value dims).  Launched as a programmatic
+// thread per (token, head, 4 value dims).  Launched as a programmatic
 // dependent of the attention launch: nothing is read before the wait.  The
-// loop over groups issues the loads of four groups before using any, so
-// their latencies overlap.
+// groups are taken eight at a time, every load of the eight issued before
+// any is used (one memory round trip for Sg <= 8); the running maximum is
+// moved between batches by rescaling what has been summed.
+constexpr int kCombineUnits = kDim / 4;         // 4-dim units per head
+constexpr int kCombineBatch = 8;
 __global__ void __launch_bounds__(256) dsv4_combine_kernel(const __grid_constant__ Params p) {
-    const int nb = (p.H * 64 + 255) / 256;                      // blocks per token
+    const int nb = (p.H * kCombineUnits + 255) / 256;          // blocks per token
     const int t = blockIdx.x / nb;
-    const int it = (blockIdx.x % nb) * blockDim.x + threadIdx.x;   // (head, 8-dim unit)
+    const int it = (blockIdx.x % nb) * blockDim.x + threadIdx.x;   // (head, 4-dim unit)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (it >= p.H * 64) return;
-    const int h = it >> 6;
-    const int u = it & 63;
+    if (it >= p.H * kCombineUnits) return;
+    const int h = it / kCombineUnits;
+    const int u = it % kCombineUnits;
     const int Sg = p.gsplits;
     const float sk = p.sink[h] * kLog2e;
     const float2* mlp = p.part_ml + (size_t)t * Sg * p.H + h;
-    const float* src = p.part_o + ((size_t)t * Sg * p.H + h) * kDim + u * 8;
+    const float* src = p.part_o + ((size_t)t * Sg * p.H + h) * kDim + u * 4;
     const size_t gstride = (size_t)p.H * kDim;
-    float M = sk;
-    for (int g = 0; g < Sg; ++g) M = fmaxf(M, mlp[(size_t)g * p.H].x);
-    float L = (M != -INFINITY && sk != -INFINITY) ? exp2f(sk - M) : 0.f;
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (M != -INFINITY) {
-        for (int g0 = 0; g0 < Sg; g0 += 4) {
-            float w[4];
-            float4 a[4], b[4];
+    float M = sk;                                   // running maximum (log2 units)
+    float L = sk != -INFINITY ? 1.f : 0.f;          // exp2(sink - M)
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int g0 = 0; g0 < Sg; g0 += kCombineBatch) {
+        float2 ml[kCombineBatch];
+        float4 o[kCombineBatch];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int g = g0 + k;
-                w[k] = 0.f;
-                a[k] = b[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (g < Sg) {
-                    const float2 v = mlp[(size_t)g * p.H];
-                    if (v.x != -INFINITY && v.y > 0.f) {
-                        w[k] = v.y * exp2f(v.x - M);
-                        a[k] = *reinterpret_cast<const float4*>(src + g * gstride);
-                        b[k] = *reinterpret_cast<const float4*>(src + g * gstride + 4);
-                    }
-                }
+        for (int k = 0; k < kCombineBatch; ++k) {
+            const int g = g0 + k;
+            ml[k] = make_float2(-INFINITY, 0.f);
+            o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (g < Sg) {
+                ml[k] = mlp[(size_t)g * p.H];
+                o[k] = *reinterpret_cast<const float4*>(src + g * gstride);
             }
+        }
+        float mb = M;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                L += w[k];
-                acc[0] += w[k] * a[k].x; acc[1] += w[k] * a[k].y; acc[2] += w[k] * a[k].z; acc[3] += w[k] * a[k].w;
-                acc[4] += w[k] * b[k].x; acc[5] += w[k] * b[k].y; acc[6] += w[k] * b[k].z; acc[7] += w[k] * b[k].w;
-            }
+        for (int k = 0; k < kCombineBatch; ++k)
+            if (ml[k].y > 0.f) mb = fmaxf(mb, ml[k].x);
+        if (mb == -INFINITY) continue;              // nothing in this batch, nor before it
+        if (mb > M) {
+            const float r = M == -INFINITY ? 0.f : exp2f(M - mb);
+            L *= r;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[j] *= r;
+            M = mb;
+        }
+#pragma unroll
+        for (int k = 0; k < kCombineBatch; ++k) {
+            const float w = ml[k].y > 0.f ? ml[k].y * exp2f(ml[k].x - M) : 0.f;
+            L += w;
+            acc[0] += w * o[k].x;
+            acc[1] += w * o[k].y;
+            acc[2] += w * o[k].z;
+            acc[3] += w * o[k].w;
         }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    uint4 v;
+    uint2 v;
     v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
     v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-    v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    *reinterpret_cast<uint4*>(p.out + ((size_t)t * p.H + h) * kDim + u * 8) = v;
+    *reinterpret_cast<uint2*>(p.out + ((size_t)t * p.H + h) * kDim + u * 4) = v;
     if (u == 0 && p.lse) p.lse[(size_t)t * p.H + h] = (L > 0.f ? M + log2f(L) : -INFINITY) * kLn2;
 }
 
@@ -1456,7 +1465,7 @@ static int run(const Call& c) {
     if (sg > 1) {
         cudaLaunchConfig_t ccfg = {};
         cudaLaunchAttribute cattr[1];
-        ccfg.gridDim = dim3(static_cast<unsigned>((c.H * 64 + 255) / 256 * c.T), 1, 1);
+        ccfg.gridDim = dim3(static_cast<unsigned>((c.H * kCombineUnits + 255) / 256 * c.T), 1, 1);
         ccfg.blockDim = dim3(256, 1, 1);
         ccfg.dynamicSmemBytes = 0;
         ccfg.stream = st;
