@@ -181,15 +181,63 @@ def oracle_throughput(inp_cpu, workers, seconds, per_task=4):
     return best, rounds * workers * per_task
 
 
-def hold_stream(stream, cycles=2_000_000):
+def capture_steps(step, R, steps, stream):
+    """CUDA graphs that together replay `steps` calls, call k on input set
+    k % R.  A short run is one graph (no graph boundary inside the timed
+    region); a long one is a graph of whole rotations (about 256 calls)
+    replayed as often as it fits, plus a graph of the remainder.  Returns
+    the replay plan [(graph, times), ...] and (graph, calls) for warming the
+    clocks."""
+    import torch
+
+    def cap(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(n):
+                step(k, torch.cuda.current_stream())
+        return g
+
+    if steps <= 512:
+        g = cap(steps)
+        return [(g, 1)], (g, steps)
+    block = R * max(1, 256 // R)
+    full, rem = divmod(steps, block)
+    g = cap(block)
+    plan = [(g, full)]
+    if rem:
+        plan.append((cap(rem), 1))
+    return plan, (g, block)
+
+
+def capture_lead(step, R, stream):
+    """A one-call graph on the last input set, run right before the timed
+    region so that the switch from the spin kernel to the measured kernel
+    (its shared-memory configuration, its first launch) happens outside it;
+    the first timed call (set 0) was last touched a whole rotation earlier."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step(R - 1, torch.cuda.current_stream())
+    return g
+
+
+def replay(plan):
+    for g, times in plan:
+        for _ in range(times):
+            g.replay()
+
+
+def hold_stream(stream, lead=None, cycles=2_000_000):
     """Keep the launch stream busy for a fixed number of GPU cycles (about
     1 ms; the spin reads nothing and waits on nothing) so that the host has
     enqueued the timed graph replays before the first of them starts: the
     timed region then holds the kernels back to back, not the host's launch
-    latency."""
+    latency.  `lead` (a graph) runs after the spin, before the timed region."""
     import torch
     with torch.cuda.stream(stream):
         torch.cuda._sleep(cycles)
+        if lead is not None:
+            lead.replay()
 
 
 class ClockSampler:
@@ -474,17 +522,8 @@ def run_store(args):
     torch.cuda.synchronize()
     if attn.dsv4_attn_get_device_error(stream) != 0:
         raise RuntimeError("device error flags set during warm-up")
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for k in range(R):
-            step(k, torch.cuda.current_stream())
-    full, rem = divmod(args.steps, R)
-    tail = None
-    if rem:
-        tail = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(tail, stream=stream):
-            for k in range(rem):
-                step(k, torch.cuda.current_stream())
+    plan, (graph, gcalls) = capture_steps(step, R, args.steps, stream)
+    lead = capture_lead(step, R, stream)
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
@@ -492,7 +531,7 @@ def run_store(args):
         clocks.start()
         time.sleep(0.5)
         with torch.cuda.stream(stream):
-            for _ in range(max(1, int(0.5 / max(1e-6, 20e-6 * R)))):
+            for _ in range(max(1, int(0.5 / max(1e-6, 20e-6 * gcalls)))):
                 graph.replay()
         torch.cuda.synchronize()
     if world > 1:
@@ -500,13 +539,10 @@ def run_store(args):
     torch.cuda.synchronize()
     clocks.mark()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    hold_stream(stream)
+    hold_stream(stream, lead)
     ev0.record(stream)
     with torch.cuda.stream(stream):
-        for _ in range(full):
-            graph.replay()
-        if tail is not None:
-            tail.replay()
+        replay(plan)
     ev1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -599,7 +635,7 @@ def run_store(args):
                    "rows_per_request": w.rows_per_request, "kv_format": w.kv_format, "input_sets": R,
                    "l2": f"inputs larger than L2: {R} rotating sets with their own pools "
                          f"({R * nbytes / 1e6:.0f} MB touched per rotation vs L2 {l2 / 1e6:.0f} MB)",
-                   "timing": "CUDA graph replays of one call per input set, CUDA events on the launch stream"},
+                   "timing": "CUDA-graph replays (one graph for runs of up to 512 steps, else graphs of whole rotations of about 256 calls), step k on input set k mod sets, CUDA events on the launch stream after a 1 ms device spin"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(args.workload),
@@ -654,24 +690,15 @@ def run_topk(args):
     torch.cuda.synchronize()
     if attn.dsv4_attn_get_device_error(stream) != 0:
         raise RuntimeError("device error flags set during warm-up")
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(R):
-            step(i, torch.cuda.current_stream())
-    full, rem = divmod(args.steps, R)
-    tail = None
-    if rem:
-        tail = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(tail, stream=stream):
-            for i in range(rem):
-                step(i, torch.cuda.current_stream())
+    plan, (graph, gcalls) = capture_steps(step, R, args.steps, stream)
+    lead = capture_lead(step, R, stream)
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     if not args.quick:
         clocks.start()
         time.sleep(0.5)
         with torch.cuda.stream(stream):
-            for _ in range(max(1, int(0.5 / max(1e-6, 10e-6 * R)))):
+            for _ in range(max(1, int(0.5 / max(1e-6, 10e-6 * gcalls)))):
                 graph.replay()
         torch.cuda.synchronize()
     if world > 1:
@@ -679,13 +706,10 @@ def run_topk(args):
     torch.cuda.synchronize()
     clocks.mark()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    hold_stream(stream)
+    hold_stream(stream, lead)
     ev0.record(stream)
     with torch.cuda.stream(stream):
-        for _ in range(full):
-            graph.replay()
-        if tail is not None:
-            tail.replay()
+        replay(plan)
     ev1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -768,7 +792,7 @@ def run_topk(args):
                    "input_sets": R,
                    "l2": f"inputs larger than L2: {R} rotating sets ({R * nbytes / 1e6:.0f} MB touched per "
                          f"rotation vs L2 {l2 / 1e6:.0f} MB)",
-                   "timing": "CUDA graph replays of one call per input set, CUDA events on the launch stream"},
+                   "timing": "CUDA-graph replays (one graph for runs of up to 512 steps, else graphs of whole rotations of about 256 calls), step k on input set k mod sets, CUDA events on the launch stream after a 1 ms device spin"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(args.workload),
@@ -820,29 +844,17 @@ def measure_workload(args, workload, dev, world, steps):
             step(k, stream)
     torch.cuda.synchronize()
     R = len(sets)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for k in range(R):
-            step(k, torch.cuda.current_stream())
-    full, rem = divmod(steps, R)
-    tail = None
-    if rem:
-        tail = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(tail, stream=stream):
-            for k in range(rem):
-                step(k, torch.cuda.current_stream())
+    plan, (graph, gcalls) = capture_steps(step, R, steps, stream)
+    lead = capture_lead(step, R, stream)
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    hold_stream(stream)
+    hold_stream(stream, lead)
     ev0.record(stream)
     with torch.cuda.stream(stream):
-        for _ in range(full):
-            graph.replay()
-        if tail is not None:
-            tail.replay()
+        replay(plan)
     ev1.record(stream)
     torch.cuda.synchronize()
     ms = slowest_ms(ev0.elapsed_time(ev1), world, dev)
@@ -923,17 +935,8 @@ def run_ours(args):
 
     # ---- one CUDA graph holds one call per input set; replays cover K steps
     R = len(sets)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for k in range(R):
-            step(k, torch.cuda.current_stream())
-    full, rem = divmod(args.steps, R)
-    tail = None
-    if rem:
-        tail = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(tail, stream=stream):
-            for k in range(rem):
-                step(k, torch.cuda.current_stream())
+    plan, (graph, gcalls) = capture_steps(step, R, args.steps, stream)
+    lead = capture_lead(step, R, stream)
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
@@ -942,7 +945,7 @@ def run_ours(args):
         time.sleep(0.5)
         # spin the GPU for a moment so the clock samples see it under load
         with torch.cuda.stream(stream):
-            for _ in range(max(1, int(0.5 / max(1e-6, 6e-6 * R)))):
+            for _ in range(max(1, int(0.5 / max(1e-6, 6e-6 * gcalls)))):
                 graph.replay()
         torch.cuda.synchronize()
     if world > 1:
@@ -950,13 +953,10 @@ def run_ours(args):
     torch.cuda.synchronize()
     clocks.mark()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    hold_stream(stream)
+    hold_stream(stream, lead)
     ev0.record(stream)
     with torch.cuda.stream(stream):
-        for _ in range(full):
-            graph.replay()
-        if tail is not None:
-            tail.replay()
+        replay(plan)
     ev1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -1065,7 +1065,7 @@ def run_ours(args):
                    "l2": f"inputs larger than L2: {R} rotating sets with their own pools "
                          f"({R * nbytes / 1e6:.0f} MB touched per rotation vs L2 {l2 / 1e6:.0f} MB)",
                    "split_plan": {"cluster_splits": sc, "grid_splits": sg},
-                   "timing": "CUDA graph replays of one call per input set, CUDA events on the launch stream"},
+                   "timing": "CUDA-graph replays (one graph for runs of up to 512 steps, else graphs of whole rotations of about 256 calls), step k on input set k mod sets, CUDA events on the launch stream after a 1 ms device spin"},
         "gpu_launches": args.steps * launches_per_step,
         "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
