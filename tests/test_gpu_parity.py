@@ -209,6 +209,13 @@ def test_fp8_h128(attn):
     run_and_compare(attn, small("c128", 128, (700, 3000), kv_format="fp8", seed=81))
 
 
+@pytest.mark.parametrize("kind,splits", [("c4", 8), ("c4", 16), ("c128", 6), ("c128", 14)])
+def test_fp8_split_merge(attn, kind, splits):
+    # packed-FP8 rows (values up to a few units) through the cluster merge's
+    # bf16 exchange and, past 8 slices, the combine kernel's fp32 partials
+    run_and_compare(attn, small(kind, 64, (2000, 9000), qlen=2, kv_format="fp8", seed=82), num_splits=splits)
+
+
 def test_full_size_c4_verify_fp8(attn):
     inp = synth.make_inputs("c4_verify_fp8", device="cuda")
     # every request's first and last query token, and all four of every 8th request
