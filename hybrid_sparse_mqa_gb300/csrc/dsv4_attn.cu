@@ -817,12 +817,15 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
             mbar_arrive(bar(B_S_FREE));
             wait_bar<kOutOfLineWait>(bar(B_MASK_FULL + stage), use & 1, abort_flag);
             const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + OFF_MASK + stage * 8) >> par;
-            float tmax = -INFINITY;
+            // four independent partial maxima and sums keep the dependent
+            // chains short
+            float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int j = 0; j < kJ; ++j) {
                 s[j] = ((mask >> (2 * j)) & 1ull) ? s[j] * p.scale_log2 : -INFINITY;
-                tmax = fmaxf(tmax, s[j]);
+                tm[j & 3] = fmaxf(tm[j & 3], s[j]);
             }
+            float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
             const bool need = live && tmax > m_run + kRescaleLog2;
             float alpha = 1.f;
@@ -831,16 +834,16 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
                 m_run = tmax;
             }
             float pv[kJ];
-            float lsum = 0.f;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
             const bool any = live && m_run != -INFINITY;
 #pragma unroll
             for (int j = 0; j < kJ; ++j) {
                 // the denominator sums the fp32 probabilities; the bf16 copies
                 // only feed the PV product
                 pv[j] = any ? fast_exp2(s[j] - m_run) : 0.f;
-                lsum += pv[j];
+                ls[j & 3] += pv[j];
             }
-            l_run = l_run * alpha + lsum;
+            l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
             // bf16 words (key 2w, key 2w + 1) of the head's line: the even-key
             // thread builds words 0..kW-1, the odd-key thread words kW..2kW-1
             uint32_t wd[kW];
