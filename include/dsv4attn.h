@@ -81,7 +81,8 @@ extern "C" {
 /* ---- status codes (return values) ---- */
 #define DSV4_OK                 0
 #define DSV4_ERR_INVALID      (-1)  /* null pointer, H outside 1..128, T/batch < 1, bad stride */
-#define DSV4_ERR_UNSUPPORTED  (-2)  /* page_size != 256, ratio not 0/4/128, row_bytes mis-sized */
+#define DSV4_ERR_UNSUPPORTED  (-2)  /* page_size != 256, ratio not 0/4/128, row_bytes mis-sized, or
+                                       more than 2^31 - 1 CTAs (tokens x key slices x 64-head groups) */
 #define DSV4_ERR_WORKSPACE    (-3)  /* workspace smaller than dsv4_attn_workspace_size() */
 #define DSV4_ERR_CUDA         (-4)  /* a CUDA runtime call or launch failed */
 #define DSV4_ERR_SCRATCH_LIMIT (-5) /* dsv4_attn_c4_sparse_noalloc: the call needs more scratch than
