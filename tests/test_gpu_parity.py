@@ -80,7 +80,7 @@ def test_swa_decode_boundaries(attn, heads):
     run_and_compare(attn, small("swa", heads, (1, 7, 127, 128, 129, 255, 256, 257, 300, 1000), seed=heads))
 
 
-@pytest.mark.parametrize("heads", [16, 64, 128])
+@pytest.mark.parametrize("heads", [1, 16, 64, 96, 128])
 def test_c4_decode_small(attn, heads):
     # no compressed row visible yet (lengths 1 and 3: every index slot is
     # absent), n_c(p) below and above topk (short lists are padded with -1)
@@ -207,6 +207,11 @@ def test_fp8_small(attn, kind, qlen):
 
 def test_fp8_h128(attn):
     run_and_compare(attn, small("c128", 128, (700, 3000), kv_format="fp8", seed=81))
+
+
+def test_fp8_h96_verify(attn):
+    # a partial second head group, several query tokens per request
+    run_and_compare(attn, small("c4", 96, (800, 6000), qlen=3, kv_format="fp8", seed=83))
 
 
 @pytest.mark.parametrize("kind,splits", [("c4", 8), ("c4", 16), ("c128", 6), ("c128", 14)])
