@@ -58,12 +58,12 @@ def run_and_compare(A, inp, *, tokens=None, num_splits=0, check_rows=True):
     return out, lse, float(err.max())
 
 
-def small(kind, heads, seq_lens, *, qlen=1, topk=512, kv_format="bf16", seed=0, rpi=None, sink=None):
+def small(kind, heads, seq_lens, *, qlen=1, topk=512, kv_format="bf16", seed=0, rpi=None, sink=None, window=128):
     ratio = dict(swa=0, c4=4, c128=128)[kind]
     inp = synth.make_inputs(
         synth.Workload(f"t_{kind}", batch=len(seq_lens), heads=heads, ratio=ratio,
                        seq_lens=tuple(seq_lens), qlen=qlen, topk=topk, kv_format=kv_format,
-                       req_pool_indices=rpi, seed=seed), device="cuda")
+                       req_pool_indices=rpi, window=window, seed=seed), device="cuda")
     if sink is not None:
         inp.sink.fill_(sink)
     return inp
@@ -85,6 +85,15 @@ def test_c4_decode_small(attn, heads):
     # no compressed row visible yet (lengths 1 and 3: every index slot is
     # absent), n_c(p) below and above topk (short lists are padded with -1)
     run_and_compare(attn, small("c4", heads, (1, 3, 4, 100, 515, 2048, 2049, 9000), seed=10 + heads))
+
+
+@pytest.mark.parametrize("kind,window", [("swa", 1), ("swa", 64), ("swa", 200), ("swa", 512),
+                                         ("c4", 64), ("c4", 200), ("c4", 512), ("c128", 300)])
+def test_window_sizes(attn, kind, window):
+    # windows shorter than a tile, spanning several index chunks (192 slots),
+    # and longer than the C4 list
+    run_and_compare(attn, small(kind, 64, (2, 150, 700, 3000), qlen=2, window=window, seed=window),
+                    num_splits=0)
 
 
 @pytest.mark.parametrize("topk", [16, 100, 512])
