@@ -13,17 +13,20 @@
 // * Per 48-key tile: eight loader warps resolve key slots to pool rows (SWA
 //   page table, C4 index list, C128 range) one 192-slot chunk ahead of use and
 //   gather the 1 KB rows with 16-byte cp.async into a 128-byte-swizzled shared
-//   tile.  Two MMA warps compute S = Q K^T on tcgen05, each over one half of
-//   the 512 dims into its own fp32 TMEM accumulator (M = 64 heads, N = 48
-//   keys).  Four softmax warps read S with the 16-lane TMEM access shape: the
-//   two threads t and t ^ 2 hold the even and odd key columns of one head, so
-//   the online softmax (lazily updated running max, fp32 denominator) needs
-//   one shuffle per reduction; the bf16 probabilities go into the head's
-//   128-byte line.  A third MMA warp accumulates O^T += V^T P^T (M = 128 of
-//   the 512 value dims per MMA, N = 64 heads, K = 48 keys) into 4 x 64 TMEM
-//   columns; V is the same shared tile read MN-major (K and V are the same
-//   row).  Each tcgen05.mma costs its issuing thread about as long as a small
-//   MMA takes to run, so the products are issued from three warps and overlap.
+//   tile (packed FP8 rows: two of the warps bulk-copy the 608-byte rows two
+//   tiles ahead into the top of the stage, six dequantise them in place).
+//   Four MMA issuer warps each compute one quarter of S = Q K^T on tcgen05
+//   (128 of the 512 dims, M = 64 heads, N = 48 keys) into its own fp32 TMEM
+//   accumulator, and one 128-dim block of O^T += V^T P^T (M = 128 value dims,
+//   N = 64 heads, K = 48 keys) into 4 x 64 TMEM columns; V is the same shared
+//   tile read MN-major (K and V are the same row).  Each tcgen05.mma costs its
+//   issuing thread about as long as a small MMA takes to run, so the products
+//   are issued from four warps and overlap.  Four softmax warps read the four
+//   score quarters with the 16-lane TMEM access shape and add them: the two
+//   threads t and t ^ 2 hold the even and odd key columns of one head, so the
+//   online softmax (lazily updated running max, fp32 denominator) needs one
+//   shuffle per reduction; the bf16 probabilities go into the head's 128-byte
+//   line.
 // * At the end the sink adds exp(sink - M) to each head's denominator, the
 //   slices are merged with log-sum-exp weights and the bf16 output written.
 //
@@ -380,14 +383,14 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     // Launched as a programmatic dependent of the previous kernel in the
     // stream: barrier set-up and the TMEM allocation overlap its tail; every
     // read of an input waits for its completion.  The barriers are set up by
-    // the PV issuer warp, idle until the first probabilities, so that the
+    // an MMA issuer warp, idle until the first tile lands, so that the
     // threads whose loads start the gather are not delayed by it.
     if (tid == (kMmaWarp0 + 2) * 32) {
         mbar_init(bar(B_Q_FULL), kSoftmaxWarps * 32);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(B_KV_FULL + s), KV_FORMAT == DSV4_KV_BF16 ? kLoadThreads : kFp8DqThreads);
             mbar_init(bar(B_KV_EMPTY + s), kMmaWarps);     // every value tile's PV
-            mbar_init(bar(B_MASK_FULL + s), KV_FORMAT == DSV4_KV_BF16 ? 1 : 2);   // FP8: one per issuer warp
+            mbar_init(bar(B_MASK_FULL + s), KV_FORMAT == DSV4_KV_BF16 ? 1 : 2);   // FP8: one per copier warp
             mbar_init(bar(B_RAW_FULL + s), 2);
         }
         mbar_init(bar(B_S_FULL), kMmaWarps);                // every dim quarter of S
