@@ -111,15 +111,17 @@ def test_verify_small(attn, kind):
     run_and_compare(attn, small(kind, 64, (300, 1029, 5000), qlen=3, seed=30))
 
 
-@pytest.mark.parametrize("kind", ["swa", "c4", "c128"])
-def test_extend_chunks(attn, kind):
+@pytest.mark.parametrize("kind,chunks", [("swa", (257, 1, 130)), ("c4", (257, 1, 130)), ("c128", (257, 1, 130)),
+                                         ("c4", (5, 0, 130)), ("swa", (0, 64, 0))])
+def test_extend_chunks(attn, kind, chunks):
     # sparse prefill / extend: requests appending chunks of 1..257 tokens,
-    # ragged, across page and window boundaries (every token checked)
+    # ragged, across page and window boundaries (every token checked); a
+    # request may bring no query token at all
     work = synth.Workload(f"extend_{kind}", batch=3, heads=64, ratio={"swa": 0, "c4": 4, "c128": 128}[kind],
                           seq_lens=(300, 2000, 9000), qlen=1, swa_resident="all", seed=33)
     inp = synth.make_inputs(work)
-    # replace the one-token boundaries by ragged extend chunks of 257, 1 and 130 tokens
-    cu = torch.tensor([0, 257, 258, 388], dtype=torch.int32)
+    # replace the one-token boundaries by the ragged extend chunks
+    cu = torch.tensor([0] + list(np.cumsum(chunks)), dtype=torch.int32)
     T = int(cu[-1])
     g = torch.Generator().manual_seed(34)
     inp.cu_seqlens_q = cu
