@@ -179,6 +179,40 @@ def test_device_errors_are_flagged_not_trapped(attn):
     assert err <= TOL_MAX_BF16
 
 
+def test_position_and_extra_page_errors(attn):
+    # a request with no tokens yet (seq_len 0: its decode position is -1) and
+    # a C4 index on an extra page id past the pool: both flagged, and the
+    # outputs still match the oracle's (the position-less token attends to the
+    # sink alone: zero output, lse = sink)
+    inp = small("c4", 64, (900, 3000, 5000), seed=71)
+    from dataclasses import replace
+    seq = inp.seq_lens.clone()
+    seq[0] = 0
+    ept = inp.extra_page_table.clone()
+    i2 = int(inp.topk_idx[2, 0])
+    ept[2, i2 // 256] = inp.extra_pool.shape[0] // 256
+    bad = replace(inp, seq_lens=seq, extra_page_table=ept)
+    out, lse = attn.run_inputs(bad)
+    torch.cuda.synchronize()
+    flags = attn.dsv4_attn_get_device_error()
+    assert flags == attn.DEV_ERR["EXTRA_PAGE"] | attn.DEV_ERR["POSITION"], hex(flags)
+    res = O.dsv4_attention(**bad.oracle_kwargs())
+    assert res.errors == (O.ERR_EXTRA_PAGE | O.ERR_TOKEN_POSITION)
+    assert np.abs(out.float().cpu().numpy() - res.out).max() <= TOL_MAX_BF16
+    assert np.abs(lse.cpu().numpy() - res.lse).max() <= TOL_LSE
+
+
+def test_req_row_error(attn):
+    # a req_pool_indices entry past the page tables is flagged, not trapped
+    inp = small("c4", 32, (900, 3000), rpi=(5, 9), seed=72)
+    from dataclasses import replace
+    rpi = inp.req_pool_indices.clone()
+    rpi[1] = inp.swa_page_table.shape[0] + 3
+    attn.run_inputs(replace(inp, req_pool_indices=rpi))
+    torch.cuda.synchronize()
+    assert attn.dsv4_attn_get_device_error() & attn.DEV_ERR["REQ_ROW"]
+
+
 # ---------------------------------------------------------------- full-size workloads
 @pytest.mark.parametrize("name,tokens", [
     ("swa_decode", None),                        # every token
