@@ -213,6 +213,19 @@ def test_req_row_error(attn):
     assert attn.dsv4_attn_get_device_error() & attn.DEV_ERR["REQ_ROW"]
 
 
+def test_plan_too_short_is_flagged(attn):
+    # C128 with max_seq_len below a request's length: the plan covers fewer
+    # key slots than that token has; the call is flagged, nothing traps, and
+    # the library stays usable for a correct call afterwards
+    inp = small("c128", 64, (20000, 3000), seed=73)
+    swa = attn.make_pool(inp.swa_pool, inp.swa_page_table)
+    extra = attn.make_pool(inp.extra_pool, inp.extra_page_table)
+    attn.dsv4_attn_c128_dense(inp.q, inp.seq_lens, swa, extra, inp.sink, max_seq_len=4000, scale=inp.scale)
+    torch.cuda.synchronize()
+    assert attn.dsv4_attn_get_device_error() & attn.DEV_ERR["PLAN"]
+    run_and_compare(attn, inp)
+
+
 # ---------------------------------------------------------------- full-size workloads
 @pytest.mark.parametrize("name,tokens", [
     ("swa_decode", None),                        # every token
