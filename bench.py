@@ -968,6 +968,19 @@ def run_ours(args):
     sec_per_step = ms / 1e3 / args.steps
     value = job_tokens_per_s(T, world, sec_per_step)
 
+    # ---- per launch: the binding called once per step, no CUDA graph (the
+    # host's launch overhead counts wherever it exceeds the kernel's time)
+    n_eager = max(1, min(args.steps, 200))
+    torch.cuda.synchronize()
+    ea0, ea1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea0.record(stream)
+    for k in range(n_eager):
+        step(k, stream)
+    ea1.record(stream)
+    torch.cuda.synchronize()
+    eager_us = slowest_ms(ea0.elapsed_time(ea1), world, dev) * 1e3 / n_eager
+    flags |= attn.dsv4_attn_get_device_error(stream)
+
     # ---- end to end through the public API with host buffers
     pin = lambda x: x.cpu().pin_memory()
     hq = [pin(s.q) for s in sets]
@@ -1068,6 +1081,9 @@ def run_ours(args):
                    "timing": "CUDA-graph replays (one graph for runs of up to 512 steps, else graphs of whole rotations of about 256 calls), step k on input set k mod sets, CUDA events on the launch stream after a 1 ms device spin"},
         "gpu_launches": args.steps * launches_per_step,
         "roofline": roofline,
+        "per_launch": {"us_per_call": eager_us, "calls": n_eager,
+                       "timing": "eager calls of the Python binding one after another on the launch stream, "
+                                 "no CUDA graph; CUDA events"},
         "e2e": {"value": e2e_value, "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "cpu_baseline": cpu_baseline,
