@@ -181,6 +181,19 @@ def oracle_throughput(inp_cpu, workers, seconds, per_task=4):
     return best, rounds * workers * per_task
 
 
+def rotating_sets(make, first_bytes, requested, l2):
+    """Input sets for the timed rotation: `requested` if given (> 0), else
+    at least 12 and enough that one rotation touches four times the L2
+    (at most 512).  `make(r)` builds set r; `first_bytes(set)` is a call's
+    algorithmic bytes."""
+    first = make(0)
+    if requested > 0:
+        n = requested
+    else:
+        n = max(12, min(512, math.ceil(4 * l2 / max(1, first_bytes(first)))))
+    return [first] + [make(r) for r in range(1, n)]
+
+
 def capture_steps(step, R, steps, stream):
     """CUDA graphs that together replay `steps` calls, call k on input set
     k % R.  A short run is one graph (no graph boundary inside the timed
@@ -503,8 +516,8 @@ def run_store(args):
     from hybrid_sparse_mqa_gb300 import attn, synth
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    sets = [synth.make_store_inputs(args.workload, device=dev, seed=2000 * (rank + 1) + r)
-            for r in range(args.sets)]
+    sets = rotating_sets(lambda r: synth.make_store_inputs(args.workload, device=dev, seed=2000 * (rank + 1) + r),
+                         store_algorithmic_bytes, args.sets, l2)
     pools = [attn.make_pool(s.pool, s.page_table) for s in sets]
     inp0 = sets[0]
     n = inp0.k.shape[0]
@@ -671,7 +684,8 @@ def run_topk(args):
     from hybrid_sparse_mqa_gb300 import attn, synth
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    sets = [synth.make_topk_inputs(args.workload, device=dev, seed=3000 * (rank + 1) + r) for r in range(args.sets)]
+    sets = rotating_sets(lambda r: synth.make_topk_inputs(args.workload, device=dev, seed=3000 * (rank + 1) + r),
+                         topk_algorithmic_bytes, args.sets, l2)
     inp0 = sets[0]
     rows, k = inp0.scores.shape[0], inp0.work.k
     max_len = int(inp0.lengths.max())
@@ -822,7 +836,9 @@ def measure_workload(args, workload, dev, world, steps):
     import torch
     from hybrid_sparse_mqa_gb300 import attn, synth
     rank, _, _ = dist_env()
-    sets = [synth.make_inputs(workload, device=dev, seed=2000 * (rank + 1) + r) for r in range(args.sets)]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sets = rotating_sets(lambda r: synth.make_inputs(workload, device=dev, seed=2000 * (rank + 1) + r),
+                         lambda x: algorithmic_bytes_and_flops(x)[0], args.sets, l2)
     inp0 = sets[0]
     T, H = inp0.T, inp0.H
     w = inp0.work
@@ -904,9 +920,8 @@ def run_ours(args):
     # ---- rotating input sets, each with its own pools: the data one step
     # reads was last touched R steps earlier, so it is not in L2
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    sets = []
-    for r in range(args.sets):
-        sets.append(synth.make_inputs(args.workload, device=dev, seed=1000 * (rank + 1) + r))
+    sets = rotating_sets(lambda r: synth.make_inputs(args.workload, device=dev, seed=1000 * (rank + 1) + r),
+                         lambda x: algorithmic_bytes_and_flops(x)[0], args.sets, l2)
     inp0 = sets[0]
     T, H = inp0.T, inp0.H
     nbytes, flops = algorithmic_bytes_and_flops(inp0)
@@ -1105,7 +1120,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--sets", type=int, default=12)
+    ap.add_argument("--sets", type=int, default=0,
+                    help="input sets in the timed rotation (0: at least 12 and four times the L2 per rotation)")
     ap.add_argument("--num-splits", type=int, default=0,
                     help="key-list pieces per token (0 = the library's plan)")
     ap.add_argument("--e2e-steps", type=int, default=2000)
