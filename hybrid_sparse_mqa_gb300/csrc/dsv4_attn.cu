@@ -241,12 +241,26 @@ __device__ void token_info(const Params& p, int t, int split, TokenInfo& ti, uns
         trow = p.rpi ? __ldg(p.rpi + b) : b;
         pos = __ldg(p.seq_lens + b) - 1;
     } else {
-        int lo = 0, hi = p.batch - 1;        // largest b with cu[b] <= t
-        while (lo < hi) {
-            int mid = (lo + hi + 1) >> 1;
-            if (__ldg(p.cu_seqlens + mid) <= t) lo = mid; else hi = mid - 1;
+        // largest b < batch with cu[b] <= t (cu is non-decreasing, so the
+        // entries <= t are a prefix): the warp loads 256 entries at a time,
+        // every load issued before any vote, so a batch of up to 256 costs
+        // one round trip instead of a binary search's chain of loads.  Every
+        // lane of the warp calls this.
+        const int lane = threadIdx.x & 31;
+        b = 0;
+        for (int base = 0; base < p.batch; base += 256) {
+            int v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = base + 32 * j + lane;
+                v[j] = i < p.batch ? __ldg(p.cu_seqlens + i) : INT_MAX;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const unsigned m = __ballot_sync(0xffffffffu, v[j] <= t);
+                if (m) b = base + 32 * j + 31 - __clz(m);
+            }
         }
-        b = lo;
         trow = p.rpi ? __ldg(p.rpi + b) : b;
         const int c0 = __ldg(p.cu_seqlens + b), c1 = __ldg(p.cu_seqlens + b + 1);
         if (t < c0 || t >= c1) ok = false;
@@ -458,10 +472,6 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
     const uint32_t tmem = *tmem_slot;
     const int ntiles = ti.ntiles;
     if (tid == 0) DSV4_TR(1);
-    // Packed FP8: the loader warpgroups hold two tiles' raw rows, so during
-    // the key loop they take registers from the MMA issuer warpgroup (which
-    // needs few): 4 x 128 (softmax) + 8 x 176 (loaders) + 4 x 32 (issuers)
-    // warps' worth <= the 16 x 128 the CTA is launched with.
     if (is_loader) {
         // ============================================================ loader
         const int lw = lt >> 5;
