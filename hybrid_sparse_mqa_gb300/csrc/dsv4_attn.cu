@@ -230,37 +230,41 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int* abo
     else return wait_spin(bar, parity, abort_flag);
 }
 
-// Query token t -> request row, position and the slots of slice `split`.
-// In decode the request row does not depend on the position, so its load is
-// issued together with the sequence length.
-__device__ void token_info(const Params& p, int t, int split, TokenInfo& ti, unsigned& err) {
-    int b, pos, trow;
+// The request of packed query token t (verify / extend): the largest
+// b < batch with cu_seqlens[b] <= t (the entries <= t are a prefix, cu being
+// non-decreasing).  The warp loads 256 entries at a time, every load issued
+// before any vote, so a batch of up to 256 costs one round trip instead of a
+// binary search's chain of loads.  Every lane of the warp calls this.
+__device__ __forceinline__ int request_of(const Params& p, int t) {
+    const int lane = threadIdx.x & 31;
+    int b = 0;
+    for (int base = 0; base < p.batch; base += 256) {
+        int v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = base + 32 * j + lane;
+            v[j] = i < p.batch ? __ldg(p.cu_seqlens + i) : INT_MAX;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const unsigned m = __ballot_sync(0xffffffffu, v[j] <= t);
+            if (m) b = base + 32 * j + 31 - __clz(m);
+        }
+    }
+    return b;
+}
+
+// Token t (of request b, found by request_of in verify / extend) -> request
+// row, position and the slots of slice `split`.  In decode the request row
+// does not depend on the position, so its load is issued together with the
+// sequence length.
+__device__ void token_info(const Params& p, int t, int b, int split, TokenInfo& ti, unsigned& err) {
+    int pos, trow;
     bool ok = true;
     if (p.cu_seqlens == nullptr) {
-        b = t;
         trow = p.rpi ? __ldg(p.rpi + b) : b;
         pos = __ldg(p.seq_lens + b) - 1;
     } else {
-        // largest b < batch with cu[b] <= t (cu is non-decreasing, so the
-        // entries <= t are a prefix): the warp loads 256 entries at a time,
-        // every load issued before any vote, so a batch of up to 256 costs
-        // one round trip instead of a binary search's chain of loads.  Every
-        // lane of the warp calls this.
-        const int lane = threadIdx.x & 31;
-        b = 0;
-        for (int base = 0; base < p.batch; base += 256) {
-            int v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int i = base + 32 * j + lane;
-                v[j] = i < p.batch ? __ldg(p.cu_seqlens + i) : INT_MAX;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const unsigned m = __ballot_sync(0xffffffffu, v[j] <= t);
-                if (m) b = base + 32 * j + 31 - __clz(m);
-            }
-        }
         trow = p.rpi ? __ldg(p.rpi + b) : b;
         const int c0 = __ldg(p.cu_seqlens + b), c1 = __ldg(p.cu_seqlens + b + 1);
         if (t < c0 || t >= c1) ok = false;
@@ -443,21 +447,24 @@ __global__ void __launch_bounds__(kThreads, 1) dsv4_attn_kernel(const __grid_con
         lp_lo = e0n / kPageSize;
         ncache = max(0, min(p.ex_pt_stride - lp_lo, (min(p.ce, kRingHalf) + kPageSize - 1) / kPageSize + 1));
     }
-    const bool early_row = p.cu_seqlens == nullptr && p.rpi == nullptr && p.ratio != 0 && t < p.ex_pt_rows;
+    // the token's request (verify / extend: one warp-wide lookup); without
+    // req_pool_indices it is also the page-table row
+    const int b_req = p.cu_seqlens == nullptr ? t : request_of(p, t);
+    const bool early_row = p.rpi == nullptr && p.ratio != 0 && b_req < p.ex_pt_rows;
     int pre_idx = -1;
     if (is_loader) {
         if (p.ratio == 4 && lt < min(p.ce, kRingHalf) && e0n + lt < p.topk)
             pre_idx = __ldg(p.topk_idx + (size_t)t * p.topk + e0n + lt);
         if (early_row)
             for (int k = lt; k < ncache; k += kLoadThreads)
-                pt_cache[k] = __ldg(p.ex_pt + (size_t)t * p.ex_pt_stride + lp_lo + k);
+                pt_cache[k] = __ldg(p.ex_pt + (size_t)b_req * p.ex_pt_stride + lp_lo + k);
     }
     // every thread derives the token's coordinates itself (same addresses; the
     // loads overlap the barrier set-up); thread 0 reports the errors
     TokenInfo ti;
     {
         unsigned e0 = 0;
-        token_info(p, t, split, ti, e0);
+        token_info(p, t, b_req, split, ti, e0);
         if (tid == 0) err |= e0;
     }
     if (is_loader && !early_row && p.ratio != 0 && ti.ntiles > 0)
